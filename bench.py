@@ -1,0 +1,381 @@
+#!/usr/bin/env python3
+"""Benchmark of the FlashAttention-2 forward pass on GB300.
+
+One step = one forward pass (the whole path: tile scheduling, Q/K/V tile
+loads, S = Q K^T, masking, online softmax, O += P V, epilogue) over the
+headline workload, bf16 B=4 H=16 N=4096 d=128 causal, with Q, K, V resident
+in HBM.  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU
+(independent replicas: the path needs no exchange between GPUs), the timed
+region is bracketed by a barrier and a synchronize on both sides, the time
+is the max over ranks, and `value` counts the work of all ranks.
+"""
+from __future__ import annotations
+
+import os
+
+# The CPU oracle (baseline and reference legs) runs one head per worker
+# process; each worker's BLAS is single-threaded.  Must be set before numpy loads.
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import multiprocessing as mp
+import shutil
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "FA2 fwd TFLOP/s, bf16 B4 H16 N4096 d128 causal; % of GB300 dense peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20  # larger than the 129 MB L2
+KERNEL_SOURCES = ["tiled_attention_fwd_gb300/csrc/fa_fwd_tc.cuh", "tiled_attention_fwd_gb300/csrc/ptx.cuh",
+                  "tiled_attention_fwd_gb300/csrc/fa_tc_launch.cuh"]
+
+
+# ------------------------------------------------------------------ helpers
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS if k in d}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def load_traffic(workload: str):
+    """dram bytes per launch from a committed ncu summary, if it was taken on this kernel source."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{workload}.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    if d.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        exe = shutil.which("nvidia-smi")
+        if exe is not None:
+            self.out = tempfile.TemporaryFile(mode="w+")
+            self.proc = subprocess.Popen([exe, f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.out is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.out.seek(0)
+        rows = [r for r in csv.reader(io.StringIO(self.out.read())) if len(r) >= 9]
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax = float(r[2])
+            except ValueError:
+                continue
+            for n, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def aggregate_ranks(local_seconds: float, world: int, reduce_max=None) -> float:
+    """Max over ranks of the timed-region duration (identity on one rank)."""
+    if world <= 1 or reduce_max is None:
+        return local_seconds
+    return reduce_max(local_seconds)
+
+
+# ------------------------------------------------------------------ CPU oracle legs
+def _oracle_head(args):
+    import numpy as np  # noqa: F401  (worker process: BLAS single-threaded by env)
+
+    import oracle
+    q, k, v, scale, causal = args
+    t0 = time.perf_counter()
+    oracle.attention_head(q, k, v, scale, causal)
+    return time.perf_counter() - t0
+
+
+def oracle_sample(w, budget_s: float, pool, cores: int, inputs=None):
+    """Run the fp64 oracle on whole heads of workload `w` for about `budget_s`
+    seconds on `cores` worker processes; returns (TFLOP/s, heads, seconds)."""
+    from tiled_attention_fwd_gb300.inputs import as_f64_numpy, make_qkv
+
+    q, k, v = make_qkv(w) if inputs is None else inputs
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    per_head = w.flops / len(heads)
+    qn, kn, vn = as_f64_numpy(q), as_f64_numpy(k), as_f64_numpy(v)
+    t0 = time.perf_counter()
+
+    def submit(i):
+        b, h = heads[i]
+        return pool.apply_async(_oracle_head, ((qn[b, h], kn[b, h], vn[b, h], w.scale, w.causal),))
+
+    pending = [submit(i) for i in range(min(cores, len(heads)))]
+    nxt, done = len(pending), 0
+    while pending:
+        pending.pop(0).get()
+        done += 1
+        if nxt < len(heads) and time.perf_counter() - t0 < budget_s:
+            pending.append(submit(nxt))
+            nxt += 1
+    dt = time.perf_counter() - t0
+    return done * per_head / dt / 1e12, done, dt
+
+
+def make_pool(cores: int):
+    ctx = mp.get_context("spawn")
+    return ctx.Pool(cores)
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return 0
+    from tiled_attention_fwd_gb300.inputs import make_qkv
+
+    cores = os.cpu_count() or 1
+    pool = make_pool(cores)
+    inputs = make_qkv(w)
+    budget = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_sample(w, budget, pool, cores, inputs)
+    vals, heads, secs = [], 0, 0.0
+    for _ in range(args.steps):
+        v, h, s = oracle_sample(w, budget, pool, cores, inputs)
+        vals.append(v)
+        heads += h
+        secs += s
+    pool.close()
+    value = heads * (w.flops / (w.B * w.H)) / secs / 1e12
+    sample = (f"whole heads of the workload, as many as fit in ~{budget:.0f} s per step on {cores} worker "
+              f"processes (one head each, fp64, BLAS single-threaded); {heads} heads in {args.steps} steps")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": secs / max(1, args.steps) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(w):
+    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+            "dtype": w.dtype, "inputs": f"seeded iid normal (seed {w.seed}, Q/K std {w.qk_std})",
+            "l2": "flushed (256 MB write) between timed steps", "layout": "[B,H,N,d] contiguous"}
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    import tiled_attention_fwd_gb300 as fa
+    from tiled_attention_fwd_gb300.inputs import make_qkv
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    want_cpu = (not args.no_cpu_baseline) and rank == 0 and world == 1
+    cores = os.cpu_count() or 1
+    pool = make_pool(cores) if want_cpu else None  # spawn before the first GPU call
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    reduce_max = None
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+        def reduce_max(x):
+            t = torch.tensor([x], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            return float(t.item())
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    q, k, v = make_qkv(w)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    o = torch.empty_like(qd)
+    lse = torch.empty((w.B, w.H, w.N), device=dev, dtype=torch.float32)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    fn = fa.fa_fwd if w.dtype == "bf16" else fa.fa_fwd_f32
+
+    def step():
+        rc = fn(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), lse.data_ptr(), w.B, w.H, w.N, w.d,
+                w.scale, w.causal, sh)
+        if rc != 0:
+            raise fa.FAError(rc, fn.__name__)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    fa.check_status(dev)
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local) as clocks:
+        barrier()
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()  # outside the events: L2 holds no inputs when each step starts
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        barrier()
+        t_wall = time.perf_counter() - t_wall
+    fa.check_status(dev)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    local_s = sum(step_ms) / 1e3
+    total_s = aggregate_ranks(local_s, world, reduce_max)
+    value = world * args.steps * w.flops / total_s / 1e12
+    kernel_ms = statistics.mean(step_ms)
+
+    # End to end through the C ABI on HOST buffers: H2D of Q, K, V from pinned
+    # memory, the forward pass, D2H of O and L, every step.
+    e2e = None
+    if not args.no_e2e and w.dtype == "bf16":
+        qp, kp, vp = (t.pin_memory() for t in (q, k, v))
+        op = torch.empty_like(qp).pin_memory()
+        lp = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
+        nbytes = fa.fa_fwd_host_workspace_bytes(w.B, w.H, w.N, w.d)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+
+        def host_step():
+            rc = fa.fa_fwd_host(qp.data_ptr(), kp.data_ptr(), vp.data_ptr(), op.data_ptr(), lp.data_ptr(),
+                                ws.data_ptr(), nbytes, w.B, w.H, w.N, w.d, w.scale, w.causal, sh)
+            if rc != 0:
+                raise fa.FAError(rc, "fa_fwd_host")
+
+        for _ in range(max(1, args.warmup)):
+            host_step()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            host_step()
+        e1.record(stream)
+        barrier()
+        e2e_s = aggregate_ranks(e0.elapsed_time(e1) / 1e3, world, reduce_max)
+        tb = w.B * w.H * w.N * w.d * 2
+        e2e = {"value": world * args.steps * w.flops / e2e_s / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": 3 * tb, "d2h_bytes_per_step": tb + w.B * w.H * w.N * 4,
+               "ms_per_step": e2e_s / args.steps * 1e3, "api": "fa_fwd_host (C ABI, pinned host buffers)"}
+        fa.check_status(dev)
+
+    cpu = None
+    if want_cpu:
+        tflops, heads, secs = oracle_sample(w, args.cpu_seconds, pool, cores, (q, k, v))
+        cpu = {"value": tflops, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"{heads} whole heads of the workload (fp64 standard attention, one head per worker "
+                         f"process, {cores} processes, BLAS single-threaded) in {secs:.1f} s"}
+    if pool is not None:
+        pool.close()
+
+    peaks, src = load_peaks()
+    peak = peaks["bf16_tflops"]
+    achieved = w.flops / (kernel_ms / 1e3) / 1e12
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "traffic": load_traffic(w.name), "peak_source": f"bf16 dense burst, {src}",
+            "kernel": f"fa_fwd_tc_kernel<{w.d},{str(w.causal).lower()}>" if w.dtype == "bf16" else "fa_fwd_simt_kernel",
+            "flops_per_launch": w.flops}
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_s / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": config_of(w), "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": args.steps, "clocks": clocks.summary(),
+            "kernel_ms": {"mean": kernel_ms, "min": min(step_ms), "max": max(step_ms),
+                          "median": statistics.median(step_ms)},
+            "wall_s_timed_region": t_wall,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    from tiled_attention_fwd_gb300.inputs import HEADLINE, WORKLOADS
+
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=HEADLINE)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU oracle sample budget")
+    args = ap.parse_args(argv)
+    if args.impl == "ours":
+        args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

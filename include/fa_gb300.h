@@ -1,0 +1,136 @@
+/*
+ * fa_gb300.h - C ABI of the GB300 (sm_103a) FlashAttention-2 forward pass.
+ *
+ * The operation (every entry point below computes it, for each batch b and
+ * head h independently):
+ *
+ *   S = (Q K^T) * scale                         "Writing a FlashAttention kernel in Metal",
+ *                                               section "Standard attention"
+ *   causal: S[q][k] = -inf for key k > query q  same page, "Blockwise attention and causal
+ *                                               masking" (absolute positions, top-left aligned)
+ *   O = softmax_rows(S) V                       same page, "Standard attention"
+ *   L[q] = log sum_k exp(S[q][k])  (natural log; the tiled method's m + log l)
+ *                                               "FlashAttention-2 from PyTorch to Triton",
+ *                                               section "What We Are Building"
+ *
+ * The N x N matrices S and P are never stored: the kernels run the FA2
+ * recurrence of the latter page (running row max m, rescaled row sum l,
+ * unnormalised O, one division by l at the end) over key/value tiles.
+ *
+ * Layout: Q, K, V and O are [B][H][N][d] row-major and contiguous (element
+ * (b,h,n,c) at ((b*H + h)*N + n)*d + c); L is [B][H][N] fp32.  N_q = N_k = N.
+ *
+ * Ownership: the caller allocates and owns every buffer passed in.  The
+ * library keeps one small device status word per device (allocated on the
+ * first call on that device, never freed before process exit).
+ *
+ * Asynchrony: every call only enqueues work on `stream` (a cudaStream_t
+ * passed as void*, NULL = legacy default stream) and returns without
+ * synchronising.  Argument errors are detected on the host before anything is
+ * enqueued.  A device-side wait that exceeds its time limit ends the kernel
+ * early and records FA_ERR_TIMEOUT in the device status word, which
+ * fa_status() reports.
+ *
+ * Return codes: FA_OK (0) or one of the negative FA_ERR_* values below;
+ * fa_strerror() names them.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  FA_OK = 0,
+  FA_ERR_NULL_POINTER = -1,   /* a required pointer is NULL                                  */
+  FA_ERR_BAD_SHAPE = -2,      /* B, H or N < 1, or B*H*N*d does not fit the index types      */
+  FA_ERR_UNSUPPORTED_D = -3,  /* head dimension not supported by this entry point            */
+  FA_ERR_MISALIGNED = -4,     /* a device pointer is not 16-byte aligned                     */
+  FA_ERR_CUDA = -5,           /* a CUDA runtime or driver call failed (launch, tensor map)   */
+  FA_ERR_TIMEOUT = -6,        /* a bounded device-side wait expired (reported by fa_status)  */
+  FA_ERR_ARCH = -7,           /* the current device is not a compute capability 10.3 GPU     */
+  FA_ERR_BAD_SCALE = -8,      /* scale is not a finite number > 0                            */
+  FA_ERR_WORKSPACE = -9       /* the workspace passed to fa_fwd_host is too small            */
+};
+
+/*
+ * fa_fwd - bf16 forward pass on the tensor cores (tcgen05, TMA, TMEM).
+ *
+ *   q, k, v : device pointers to bf16 (__nv_bfloat16) [B][H][N][d], 16-byte aligned.
+ *   o       : device pointer to bf16 [B][H][N][d], 16-byte aligned; fully overwritten.
+ *   lse     : device pointer to fp32 [B][H][N]; fully overwritten with L (natural log).
+ *   B, H, N : batch, heads, sequence length; each >= 1.  Any N (ragged tails are masked).
+ *   d       : head dimension, one of 32, 64, 128, 256.
+ *   scale   : softmax scale applied to Q K^T (the pages use 1/sqrt(d)); finite and > 0.
+ *   causal  : nonzero applies the causal mask (key k visible to query q iff k <= q).
+ *   stream  : cudaStream_t (as void*) the work is enqueued on.
+ *
+ * Arithmetic: bf16 products with fp32 accumulation for Q K^T and P V, fp32
+ * softmax state, P rounded to bf16 before P V, O rounded to bf16 once at the end.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+           int B, int H, int N, int d, float scale, int causal, void* stream);
+
+/*
+ * fa_fwd_f32 - fp32 forward pass on the CUDA cores (SIMT), all arithmetic in fp32.
+ *
+ *   q, k, v, o : device pointers to fp32 [B][H][N][d] (4-byte aligned suffices).
+ *   lse        : device pointer to fp32 [B][H][N].
+ *   d          : any head dimension 1 <= d <= 256.
+ *   Other arguments and behaviour as fa_fwd.
+ */
+int fa_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse,
+               int B, int H, int N, int d, float scale, int causal, void* stream);
+
+/*
+ * fa_fwd_host_workspace_bytes - size of the device workspace fa_fwd_host needs
+ * for one bf16 problem of this shape (room for Q, K, V, O and L on the device,
+ * each 256-byte aligned).  Returns 0 for invalid shapes.
+ */
+size_t fa_fwd_host_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * fa_fwd_host - fa_fwd on HOST buffers: enqueues on `stream` the host-to-device
+ * copies of q, k, v into `workspace`, the forward pass, and the device-to-host
+ * copies of O and L into o and lse.  Host buffers should be page-locked for
+ * the copies to be asynchronous.  The caller synchronises `stream` before
+ * reading o and lse or reusing the inputs.
+ *
+ *   q, k, v   : host pointers to bf16 [B][H][N][d].
+ *   o, lse    : host pointers receiving bf16 O and fp32 L.
+ *   workspace : device pointer, 256-byte aligned, at least
+ *               fa_fwd_host_workspace_bytes(B, H, N, d) bytes (else FA_ERR_WORKSPACE).
+ */
+int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse,
+                void* workspace, size_t workspace_bytes,
+                int B, int H, int N, int d, float scale, int causal, void* stream);
+
+/*
+ * fa_status - synchronises `stream`, then reads and clears the device status
+ * word of the current device.  Returns FA_OK, FA_ERR_TIMEOUT if a kernel
+ * launched since the last call gave up on a bounded wait, or FA_ERR_CUDA if
+ * the synchronisation itself failed.
+ */
+int fa_status(void* stream);
+
+/*
+ * fa_set_wait_limit_ms - time limit of every device-side wait in kernels
+ * launched afterwards on any device (default 2000 ms; values < 1 are clamped
+ * to 1).  Returns the previous limit.
+ */
+int fa_set_wait_limit_ms(int ms);
+
+/* fa_strerror - static, human-readable name of a return code. */
+const char* fa_strerror(int code);
+
+/* fa_abi_version - version of this ABI (incremented on incompatible changes). */
+int fa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

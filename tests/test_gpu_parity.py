@@ -1,0 +1,119 @@
+"""CUDA path vs the fp64 oracle, element by element, on seeded inputs.
+
+Small cases compare every output; the full-size workloads run in the launch
+configuration of the benchmark and compare sampled rows that the oracle
+computes one by one, plus properties of every output.  Outputs are poisoned
+with NaN before each launch so an unwritten row fails.
+"""
+import numpy as np
+import pytest
+import torch
+
+import tiled_attention_fwd_gb300 as fa
+from tiled_attention_fwd_gb300.inputs import WORKLOADS, Workload, make_qkv
+
+from parity_util import check_full, check_sampled, run_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+def _assert(res, label):
+    assert res["ok"], f"{label}: {res}"
+
+
+# ---------------------------------------------------------------- fp32 SIMT path
+@pytest.mark.parametrize("name", ["f32_b1h1n128d16", "f32_b1h1n128d16_causal"])
+def test_f32_workload(name):
+    _assert(check_full(WORKLOADS[name]), name)
+
+
+@pytest.mark.parametrize("N,d", [(1, 16), (2, 1), (37, 7), (129, 33), (300, 64), (64, 128), (97, 256), (1000, 16)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_f32_shapes(N, d, causal):
+    w = Workload("f32_edge", 2, 3, N, d, "f32", causal, seed=100 + N + d)
+    _assert(check_full(w), f"f32 N={N} d={d} causal={causal}")
+
+
+# ---------------------------------------------------------------- bf16 tensor-core path
+@pytest.mark.parametrize("name", ["bf16_b8h1n1024d64", "bf16_b8h1n1024d64_causal"])
+def test_bf16_small_workload(name):
+    _assert(check_full(WORKLOADS[name]), name)
+
+
+@pytest.mark.parametrize("d", [32, 64, 128, 256])
+@pytest.mark.parametrize("N", [1, 127, 128, 129, 255, 256, 257, 600])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_ragged(d, N, causal):
+    w = Workload("bf16_edge", 1, 3, N, d, "bf16", causal, seed=7 * N + d)
+    _assert(check_full(w), f"bf16 N={N} d={d} causal={causal}")
+
+
+@pytest.mark.parametrize("d", [32, 64, 128, 256])
+def test_bf16_large_logits_several_units(d):
+    """Q, K ~ N(0, 3^2): large logits, the running max moves often (rescale path)."""
+    for causal in (False, True):
+        w = Workload("bf16_qk3", 2, 2, 1100, d, "bf16", causal, seed=11 + d, qk_std=3.0)
+        _assert(check_full(w), f"qk3 d={d} causal={causal}")
+
+
+def test_bf16_many_units_per_cta():
+    """More work units than SMs, so every persistent CTA runs several units."""
+    w = Workload("bf16_units", 3, 64, 700, 64, "bf16", True, seed=5)
+    _assert(check_full(w), "many units")
+
+
+@pytest.mark.parametrize("name", ["bf16_b4h16n4096d128_causal", "bf16_b1h32n16384d128_causal",
+                                  "bf16_b2h16n8192d32_qk3", "bf16_b2h16n8192d64_qk3",
+                                  "bf16_b2h16n8192d128_qk3", "bf16_b2h16n8192d256_qk3"])
+def test_full_size_sampled(name):
+    w = WORKLOADS[name]
+    heads = None
+    if w.B * w.H > 16:
+        rng = np.random.default_rng(w.seed)
+        idx = rng.choice(w.B * w.H, size=16, replace=False)
+        heads = sorted((int(i) // w.H, int(i) % w.H) for i in idx)
+    res = check_sampled(w, heads=heads)
+    print(name, res)
+    _assert(res, name)
+
+
+def test_status_clean_and_deterministic():
+    w = Workload("det", 2, 4, 777, 128, "bf16", True, seed=3)
+    q, k, v = make_qkv(w)
+    o1, l1 = run_cuda(q, k, v, True, w.scale)
+    o2, l2 = run_cuda(q, k, v, True, w.scale)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    fa.check_status()
+
+
+def test_host_buffer_entry_point_matches_device_entry_point():
+    w = Workload("host", 1, 2, 300, 64, "bf16", False, seed=9)
+    q, k, v = make_qkv(w)
+    o_dev, l_dev = run_cuda(q, k, v, w.causal, w.scale)
+    qp, kp, vp = (t.pin_memory() for t in (q, k, v))
+    o = torch.empty_like(qp).pin_memory()
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32).pin_memory()
+    nbytes = fa.fa_fwd_host_workspace_bytes(w.B, w.H, w.N, w.d)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    rc = fa.fa_fwd_host(qp.data_ptr(), kp.data_ptr(), vp.data_ptr(), o.data_ptr(), lse.data_ptr(), ws.data_ptr(),
+                        nbytes, w.B, w.H, w.N, w.d, w.scale, w.causal, stream)
+    assert rc == 0, fa.fa_strerror(rc)
+    torch.cuda.synchronize()
+    assert np.array_equal(o.double().numpy(), o_dev) and np.array_equal(lse.double().numpy(), l_dev)
+
+
+def test_argument_errors_on_device():
+    dev = torch.device("cuda", 0)
+    q = torch.zeros(1, 1, 8, 48, dtype=torch.bfloat16, device=dev)
+    with pytest.raises(fa.FAError) as e:
+        fa.forward(q, q, q)
+    assert e.value.code == -3  # d = 48 is not a tensor-core head dimension
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16, device=dev)
+    with pytest.raises(fa.FAError) as e:
+        fa.forward(q, q, q, scale=-1.0)
+    assert e.value.code == -8
+    qs = torch.zeros(1 * 1 * 8 * 64 + 1, dtype=torch.bfloat16, device=dev)[1:].view(1, 1, 8, 64)
+    with pytest.raises(fa.FAError) as e:
+        fa.forward(qs, qs, qs)
+    assert e.value.code == -4  # 2-byte offset: not 16-byte aligned

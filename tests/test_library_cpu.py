@@ -1,0 +1,100 @@
+"""The C-ABI library without a GPU: it builds for sm_103a, loads, exports every
+symbol the public header declares, and rejects bad arguments on the host
+before touching a device."""
+import ctypes
+import os
+import shutil
+
+import pytest
+
+import tiled_attention_fwd_gb300 as fa
+from tiled_attention_fwd_gb300 import _lib, build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(build.LIB) and shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+        pytest.skip("neither a built library nor nvcc is available")
+    build.build()
+    return _lib.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _lib.declared_functions()
+    assert len(names) >= 8
+    raw = ctypes.CDLL(build.LIB)
+    for n in names:
+        assert hasattr(raw, n), f"{n} declared in include/fa_gb300.h but not exported"
+        assert n in _lib._SIGNATURES, f"{n} has no Python binding"
+
+
+def test_binding_names_match_header(lib):
+    assert sorted(_lib._SIGNATURES) == _lib.declared_functions()
+
+
+def test_strerror_and_version(lib):
+    assert fa.fa_abi_version() == 1
+    assert fa.fa_strerror(0).startswith("FA_OK")
+    assert "TIMEOUT" in fa.fa_strerror(-6)
+    assert "unknown" in fa.fa_strerror(12345)
+
+
+FAKE = 1 << 20  # a 16-byte aligned non-null value; never dereferenced by these calls
+
+
+@pytest.mark.parametrize("args,code", [
+    ((0, FAKE, FAKE, FAKE, FAKE, 1, 1, 8, 64, 0.125, 0), -1),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, 0, 1, 8, 64, 0.125, 0), -2),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 0, 64, 0.125, 0), -2),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 8, 48, 0.125, 0), -3),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 8, 16, 0.125, 0), -3),
+    ((FAKE + 2, FAKE, FAKE, FAKE, FAKE, 1, 1, 8, 64, 0.125, 0), -4),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 8, 64, 0.0, 0), -8),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 8, 64, float("nan"), 1), -8),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 16, 1 << 16, 8, 64, 0.125, 0), -2),
+])
+def test_fa_fwd_rejects_bad_arguments_on_host(lib, args, code):
+    assert fa.fa_fwd(*args, None) == code
+
+
+def test_fa_fwd_f32_rejects_bad_arguments_on_host(lib):
+    assert fa.fa_fwd_f32(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 8, 257, 0.1, 0, None) == -3
+    assert fa.fa_fwd_f32(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 8, 0, 0.1, 0, None) == -3
+    assert fa.fa_fwd_f32(FAKE, FAKE, FAKE, FAKE, 0, 1, 1, 8, 16, 0.1, 0, None) == -1
+    assert fa.fa_fwd_f32(FAKE + 2, FAKE, FAKE, FAKE, FAKE, 1, 1, 8, 16, 0.1, 0, None) == -4
+    assert fa.fa_fwd_f32(FAKE, FAKE, FAKE, FAKE, FAKE, 300, 300, 8, 16, 0.1, 0, None) == -2
+
+
+def test_host_workspace_size_and_checks(lib):
+    n = fa.fa_fwd_host_workspace_bytes(2, 3, 100, 64)
+    t = 2 * 3 * 100 * 64 * 2
+    r256 = lambda x: (x + 255) // 256 * 256
+    assert n == 4 * r256(t) + r256(2 * 3 * 100 * 4)
+    assert fa.fa_fwd_host_workspace_bytes(0, 3, 100, 64) == 0
+    # too-small workspace is rejected before any copy is enqueued
+    assert fa.fa_fwd_host(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE * 16, n - 1, 2, 3, 100, 64, 0.125, 0, None) == -9
+    assert fa.fa_fwd_host(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 16, n, 2, 3, 100, 64, 0.125, 0, None) == -4
+
+
+def test_wait_limit_setting(lib):
+    prev = fa.fa_set_wait_limit_ms(1500)
+    assert prev >= 1
+    assert fa.fa_set_wait_limit_ms(0) == 1500
+    assert fa.fa_set_wait_limit_ms(prev) == 1
+
+
+def test_forward_refuses_cpu_tensors():
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.forward(q, q, q)
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    saved = _lib._lib
+    _lib._lib = None
+    try:
+        with pytest.raises(ImportError):
+            _lib.load(str(tmp_path / "nope.so"))
+    finally:
+        _lib._lib = saved

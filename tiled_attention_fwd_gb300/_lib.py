@@ -1,0 +1,160 @@
+"""ctypes binding of libfa_gb300.so: the C ABI with the same names, and a
+torch-tensor convenience wrapper.  Argument marshalling only: every step of
+the forward pass runs in the library's CUDA kernels.  There is no fallback:
+if the library is missing or fails to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libfa_gb300.so")
+HEADER = os.path.join(os.path.dirname(PKG), "include", "fa_gb300.h")
+
+_c_void_p = ctypes.c_void_p
+_c_int = ctypes.c_int
+_c_float = ctypes.c_float
+_c_size_t = ctypes.c_size_t
+
+# (name, restype, argtypes) of every entry point declared in include/fa_gb300.h
+_SIGNATURES = {
+    "fa_fwd": (_c_int, [_c_void_p] * 5 + [_c_int] * 4 + [_c_float, _c_int, _c_void_p]),
+    "fa_fwd_f32": (_c_int, [_c_void_p] * 5 + [_c_int] * 4 + [_c_float, _c_int, _c_void_p]),
+    "fa_fwd_host_workspace_bytes": (_c_size_t, [_c_int] * 4),
+    "fa_fwd_host": (_c_int, [_c_void_p] * 6 + [_c_size_t] + [_c_int] * 4 + [_c_float, _c_int, _c_void_p]),
+    "fa_status": (_c_int, [_c_void_p]),
+    "fa_set_wait_limit_ms": (_c_int, [_c_int]),
+    "fa_strerror": (ctypes.c_char_p, [_c_int]),
+    "fa_abi_version": (_c_int, []),
+}
+
+FA_OK = 0
+FA_ERR_TIMEOUT = -6
+
+_lib = None
+
+
+class FAError(RuntimeError):
+    """A nonzero return code of the C ABI."""
+
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {strerror(code)} ({code})")
+
+
+def declared_functions(header: str = HEADER):
+    """Names of the functions declared in the public header."""
+    text = open(header).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+def load(path: str = LIB_PATH):
+    """Load the shared library (once) and attach the C signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(
+            f"{path} is missing: build it with `python -m tiled_attention_fwd_gb300.build` "
+            "(or __graft_entry__.build()); there is no fallback implementation")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def strerror(code: int) -> str:
+    return load().fa_strerror(code).decode()
+
+
+def _check(rc: int, where: str):
+    if rc != FA_OK:
+        raise FAError(rc, where)
+
+
+# ---------------------------------------------------------------- C ABI, same names
+def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream) -> int:
+    """bf16 tensor-core forward; pointers are integers (device addresses)."""
+    return load().fa_fwd(q, k, v, o, lse, B, H, N, d, scale, int(bool(causal)), stream)
+
+
+def fa_fwd_f32(q, k, v, o, lse, B, H, N, d, scale, causal, stream) -> int:
+    """fp32 SIMT forward; pointers are integers (device addresses)."""
+    return load().fa_fwd_f32(q, k, v, o, lse, B, H, N, d, scale, int(bool(causal)), stream)
+
+
+def fa_fwd_host_workspace_bytes(B, H, N, d) -> int:
+    return load().fa_fwd_host_workspace_bytes(B, H, N, d)
+
+
+def fa_fwd_host(q, k, v, o, lse, workspace, workspace_bytes, B, H, N, d, scale, causal, stream) -> int:
+    """bf16 forward on host buffers (copies in, kernel, copies out, all on `stream`)."""
+    return load().fa_fwd_host(q, k, v, o, lse, workspace, workspace_bytes, B, H, N, d, scale,
+                              int(bool(causal)), stream)
+
+
+def fa_status(stream) -> int:
+    return load().fa_status(stream)
+
+
+def fa_set_wait_limit_ms(ms: int) -> int:
+    return load().fa_set_wait_limit_ms(ms)
+
+
+def fa_strerror(code: int) -> str:
+    return strerror(code)
+
+
+def fa_abi_version() -> int:
+    return load().fa_abi_version()
+
+
+# ---------------------------------------------------------------- torch convenience
+def _stream_handle(torch, device):
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None):
+    """O, L = attention forward of CUDA tensors q, k, v of shape [B, H, N, d].
+
+    bf16 inputs run the tensor-core kernel (d in {32, 64, 128, 256}); fp32
+    inputs run the SIMT kernel (1 <= d <= 256).  Returns (O, L) with O in the
+    input dtype and L fp32 [B, H, N].  Enqueued on the current stream.
+    """
+    import torch
+
+    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must share the shape [B, H, N, d]")
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("q, k, v must be CUDA tensors")
+    if not (q.dtype == k.dtype == v.dtype) or q.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("q, k, v must all be bf16 or all fp32")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("q, k, v must be contiguous [B, H, N, d]")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = d ** -0.5
+    o = torch.empty_like(q) if out is None else out
+    l = torch.empty((B, H, N), device=q.device, dtype=torch.float32) if lse is None else lse
+    with torch.cuda.device(q.device):
+        stream = _stream_handle(torch, q.device)
+        fn = fa_fwd if q.dtype == torch.bfloat16 else fa_fwd_f32
+        rc = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(), B, H, N, d,
+                float(scale), causal, stream)
+    _check(rc, fn.__name__)
+    return o, l
+
+
+def check_status(device=None):
+    """Synchronise the current stream and raise FAError if a device wait timed out."""
+    import torch
+
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        _check(fa_status(_stream_handle(torch, dev)), "fa_status")

@@ -1,0 +1,224 @@
+// C ABI of the library (declared in include/fa_gb300.h): argument checks,
+// per-device state, TMA descriptor encoding, dispatch to the kernels.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/fa_gb300.h"
+#include "fa_internal.h"
+
+namespace fa {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool ready = false;
+  int* status = nullptr;  // one device int, zeroed at creation
+  int num_sms = 0;
+  int cc_major = 0;
+  int cc_minor = 0;
+};
+
+std::mutex g_mutex;
+DeviceState g_devices[kMaxDevices];
+std::atomic<int> g_wait_limit_ms{2000};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Per-device state of the current device, created on first use.
+int current_device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& s = g_devices[dev];
+  if (!s.ready) {
+    if (cudaDeviceGetAttribute(&s.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&s.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return FA_ERR_CUDA;
+    if (s.cc_major != 10 || s.cc_minor != 3) return FA_ERR_ARCH;
+    void* p = nullptr;
+    if (cudaMalloc(&p, 256) != cudaSuccess) return FA_ERR_CUDA;
+    if (cudaMemset(p, 0, 256) != cudaSuccess) return FA_ERR_CUDA;
+    s.status = static_cast<int*>(p);
+    if (g_encode == nullptr) {
+      cudaDriverEntryPointQueryResult q;
+      void* fn = nullptr;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return FA_ERR_CUDA;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    s.ready = true;
+  }
+  *out = &s;
+  return FA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_common(int B, int H, int N, int d, float scale) {
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_BAD_SHAPE;
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh > 0x7fffffffLL) return FA_ERR_BAD_SHAPE;
+  // Work units (B*H*ceil(N/256)) and launch-grid dimensions are 32-bit ints.
+  if (bh * ((static_cast<long long>(N) + 255) / 256) > 0x7fffffffLL) return FA_ERR_BAD_SHAPE;
+  if (static_cast<long long>(N) * (d > 0 ? d : 1) * 2 >= (1LL << 40)) return FA_ERR_BAD_SHAPE;
+  if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_BAD_SCALE;
+  return FA_OK;
+}
+
+LaunchCtx make_ctx(const DeviceState& s, void* stream) {
+  LaunchCtx c;
+  c.status = s.status;
+  c.limit_ns = static_cast<unsigned long long>(g_wait_limit_ms.load()) * 1000000ull;
+  c.num_sms = s.num_sms;
+  c.stream = static_cast<cudaStream_t>(stream);
+  return c;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace
+
+int encode_bf16_map(CUtensorMap* map, const void* ptr, int BH, int N, int D, int box_cols, int box_rows,
+                    int swizzle_bytes) {
+  if (g_encode == nullptr) return -1;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(N) * D * 2};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapSwizzle swz = swizzle_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : -1;
+}
+
+}  // namespace fa
+
+extern "C" {
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+           float scale, int causal, void* stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_NULL_POINTER;
+  int rc = fa::check_common(B, H, N, d, scale);
+  if (rc != FA_OK) return rc;
+  if (d != 32 && d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED_D;
+  if (!fa::aligned16(q) || !fa::aligned16(k) || !fa::aligned16(v) || !fa::aligned16(o) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return FA_ERR_MISALIGNED;
+  fa::DeviceState* s = nullptr;
+  rc = fa::current_device_state(&s);
+  if (rc != FA_OK) return rc;
+  const fa::LaunchCtx ctx = fa::make_ctx(*s, stream);
+  const int BH = B * H;
+  const bool c = causal != 0;
+  int e = 0;
+  switch (d) {
+    case 32: e = fa::launch_tc_d32(c, q, k, v, o, lse, BH, N, scale, ctx); break;
+    case 64: e = fa::launch_tc_d64(c, q, k, v, o, lse, BH, N, scale, ctx); break;
+    case 128: e = fa::launch_tc_d128(c, q, k, v, o, lse, BH, N, scale, ctx); break;
+    default: e = fa::launch_tc_d256(c, q, k, v, o, lse, BH, N, scale, ctx); break;
+  }
+  return e == 0 ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse, int B, int H, int N, int d,
+               float scale, int causal, void* stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_NULL_POINTER;
+  int rc = fa::check_common(B, H, N, d, scale);
+  if (rc != FA_OK) return rc;
+  if (d < 1 || d > 256) return FA_ERR_UNSUPPORTED_D;
+  if (static_cast<long long>(B) * H > 65535) return FA_ERR_BAD_SHAPE;  // grid.y of the SIMT launch
+  const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o) |
+                        reinterpret_cast<uintptr_t>(lse);
+  if (mis & 3u) return FA_ERR_MISALIGNED;
+  fa::DeviceState* s = nullptr;
+  rc = fa::current_device_state(&s);
+  if (rc != FA_OK) return rc;
+  const fa::LaunchCtx ctx = fa::make_ctx(*s, stream);
+  const int e = fa::launch_simt(causal != 0, q, k, v, o, lse, B * H, N, d, scale, ctx);
+  return e == 0 ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t fa_fwd_host_workspace_bytes(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
+  const size_t elems = static_cast<size_t>(B) * H * N * d;
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  return 4 * fa::round256(elems * 2) + fa::round256(rows * 4);
+}
+
+int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
+                size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal, void* stream) {
+  if (!q || !k || !v || !o || !lse || !workspace) return FA_ERR_NULL_POINTER;
+  int rc = fa::check_common(B, H, N, d, scale);
+  if (rc != FA_OK) return rc;
+  if (d != 32 && d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED_D;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA_ERR_MISALIGNED;
+  const size_t need = fa_fwd_host_workspace_bytes(B, H, N, d);
+  if (workspace_bytes < need) return FA_ERR_WORKSPACE;
+  const size_t tbytes = static_cast<size_t>(B) * H * N * d * 2;
+  const size_t lbytes = static_cast<size_t>(B) * H * N * 4;
+  const size_t step = fa::round256(tbytes);
+  char* w = static_cast<char*>(workspace);
+  void *dq = w, *dk = w + step, *dv = w + 2 * step, *dout = w + 3 * step;
+  float* dl = reinterpret_cast<float*>(w + 4 * step);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(dq, q, tbytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(dk, k, tbytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(dv, v, tbytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return FA_ERR_CUDA;
+  rc = fa_fwd(dq, dk, dv, dout, dl, B, H, N, d, scale, causal, stream);
+  if (rc != FA_OK) return rc;
+  if (cudaMemcpyAsync(o, dout, tbytes, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaMemcpyAsync(lse, dl, lbytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return FA_OK;
+}
+
+int fa_status(void* stream) {
+  fa::DeviceState* s = nullptr;
+  int rc = fa::current_device_state(&s);
+  if (rc != FA_OK) return rc;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpy(&word, s->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+  if (word != 0) {
+    if (cudaMemset(s->status, 0, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+    return FA_ERR_TIMEOUT;
+  }
+  return FA_OK;
+}
+
+int fa_set_wait_limit_ms(int ms) {
+  if (ms < 1) ms = 1;
+  return fa::g_wait_limit_ms.exchange(ms);
+}
+
+const char* fa_strerror(int code) {
+  switch (code) {
+    case FA_OK: return "FA_OK: success";
+    case FA_ERR_NULL_POINTER: return "FA_ERR_NULL_POINTER: a required pointer is NULL";
+    case FA_ERR_BAD_SHAPE: return "FA_ERR_BAD_SHAPE: B, H or N out of range";
+    case FA_ERR_UNSUPPORTED_D: return "FA_ERR_UNSUPPORTED_D: head dimension not supported by this entry point";
+    case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED: pointer not sufficiently aligned";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA runtime or driver call failed";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a bounded device-side wait expired";
+    case FA_ERR_ARCH: return "FA_ERR_ARCH: the current device is not compute capability 10.3";
+    case FA_ERR_BAD_SCALE: return "FA_ERR_BAD_SCALE: scale must be finite and > 0";
+    case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE: workspace too small";
+    default: return "unknown fa_gb300 error code";
+  }
+}
+
+int fa_abi_version(void) { return 1; }
+
+}  // extern "C"

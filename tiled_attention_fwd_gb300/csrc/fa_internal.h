@@ -1,0 +1,42 @@
+// Internal interfaces between the C-ABI translation unit and the kernel
+// translation units (one per head dimension, plus the fp32 SIMT kernel).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+// Everything a launcher needs besides the data pointers.
+struct LaunchCtx {
+  int* status;                    // device status word of the current device
+  unsigned long long limit_ns;    // time limit of each device-side wait
+  int num_sms;                    // SMs of the current device
+  cudaStream_t stream;
+};
+
+// Encode a 3-D TMA descriptor over a contiguous bf16 [BH][N][D] tensor:
+// dimensions {D, N, BH}, box {box_cols, box_rows, 1}, swizzle span
+// `swizzle_bytes` (64 or 128).  Returns 0 on success.
+int encode_bf16_map(CUtensorMap* map, const void* ptr, int BH, int N, int D, int box_cols, int box_rows,
+                    int swizzle_bytes);
+
+// bf16 tensor-core forward for one head dimension; returns a cudaError_t-like
+// code (0 = launched).  Defined in fa_tc_d<D>.cu.
+int launch_tc_d32(bool causal, const void* q, const void* k, const void* v, void* o, float* lse, int BH, int N,
+                  float scale, const LaunchCtx& ctx);
+int launch_tc_d64(bool causal, const void* q, const void* k, const void* v, void* o, float* lse, int BH, int N,
+                  float scale, const LaunchCtx& ctx);
+int launch_tc_d128(bool causal, const void* q, const void* k, const void* v, void* o, float* lse, int BH, int N,
+                   float scale, const LaunchCtx& ctx);
+int launch_tc_d256(bool causal, const void* q, const void* k, const void* v, void* o, float* lse, int BH, int N,
+                   float scale, const LaunchCtx& ctx);
+
+// fp32 SIMT forward, 1 <= d <= 256.  Defined in fa_simt.cu.
+int launch_simt(bool causal, const float* q, const float* k, const float* v, float* o, float* lse, int BH, int N,
+                int d, float scale, const LaunchCtx& ctx);
+
+}  // namespace fa

@@ -1,0 +1,156 @@
+// fp32 forward pass on the CUDA cores (no tensor cores), for small fp32
+// problems and any head dimension 1 <= d <= 256.
+//
+// The tiled kernel of "Writing a FlashAttention kernel in Metal" (section
+// "Shared-memory tiling") stages one K/V tile in shared memory per block and
+// lets every thread run the online-softmax recurrence for its own query.
+// Here a block of 4 warps owns 16 query rows (4 per warp) and stages 32 keys
+// per tile; within a warp, lane j scores key j of the tile against the row
+// (so the row max and sum are warp shuffles), and lane c accumulates output
+// columns c, c+32, ... of the row.  State (m, l, O) is fp32, as in the
+// FlashAttention-2 forward of "FlashAttention-2 from PyTorch to Triton".
+#include <cmath>
+
+#include "fa_internal.h"
+
+namespace fa {
+
+namespace {
+
+constexpr int kSimtWarps = 4;
+constexpr int kRowsPerWarp = 4;
+constexpr int kSimtRows = kSimtWarps * kRowsPerWarp;  // query rows per block
+constexpr int kSimtKeys = 32;                          // keys per K/V tile
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// DPL: output columns per lane (ceil(d / 32) rounded up to a power of two).
+template <int DPL, bool CAUSAL>
+__global__ void __launch_bounds__(kSimtWarps * 32)
+    fa_fwd_simt_kernel(const float* __restrict__ q, const float* __restrict__ k, const float* __restrict__ v,
+                       float* __restrict__ o, float* __restrict__ lse, int N, int d, float scale) {
+  extern __shared__ float sm[];
+  const int ks = d | 1;  // odd row stride of the K tile: lane-strided reads hit distinct banks
+  float* qs = sm;                            // [kSimtRows][d]
+  float* kt = qs + kSimtRows * d;            // [kSimtKeys][ks]
+  float* vt = kt + kSimtKeys * ks;           // [kSimtKeys][d]
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const size_t head = static_cast<size_t>(blockIdx.y) * N;
+  const int row_base = blockIdx.x * kSimtRows;
+
+  for (int i = tid; i < kSimtRows * d; i += blockDim.x) {
+    const int r = row_base + i / d;
+    qs[i] = r < N ? q[(head + r) * d + i % d] : 0.f;
+  }
+
+  float m[kRowsPerWarp], l[kRowsPerWarp], acc[kRowsPerWarp][DPL];
+#pragma unroll
+  for (int i = 0; i < kRowsPerWarp; ++i) {
+    m[i] = -INFINITY;
+    l[i] = 0.f;
+#pragma unroll
+    for (int t = 0; t < DPL; ++t) acc[i][t] = 0.f;
+  }
+
+  // Key tiles wholly in the future of every row of the block are skipped.
+  int kend = N;
+  if (CAUSAL) kend = min(N, row_base + kSimtRows);
+  for (int t0 = 0; t0 < kend; t0 += kSimtKeys) {
+    __syncthreads();  // the previous tile has been read by every warp
+    for (int i = tid; i < kSimtKeys * d; i += blockDim.x) {
+      const int j = i / d, c = i % d;
+      const int key = t0 + j;
+      const bool in = key < N;
+      kt[j * ks + c] = in ? k[(head + key) * d + c] : 0.f;
+      vt[i] = in ? v[(head + key) * d + c] : 0.f;
+    }
+    __syncthreads();
+    const int key = t0 + lane;
+#pragma unroll
+    for (int i = 0; i < kRowsPerWarp; ++i) {
+      const int rl = warp * kRowsPerWarp + i;
+      const int row = row_base + rl;
+      const float* qr = qs + rl * d;
+      const float* kr = kt + lane * ks;
+      float sc = 0.f;
+      for (int c = 0; c < d; ++c) sc = fmaf(qr[c], kr[c], sc);
+      sc *= scale;
+      const bool valid = key < N && (!CAUSAL || key <= row);
+      sc = valid ? sc : -INFINITY;
+      const float m_new = fmaxf(m[i], warp_max(sc));
+      const float base = (m_new == -INFINITY) ? 0.f : m_new;
+      const float alpha = expf(m[i] - base);  // 0 on the first tile (m = -inf)
+      const float pj = expf(sc - base);       // 0 for masked keys
+      l[i] = l[i] * alpha + warp_sum(pj);
+#pragma unroll
+      for (int t = 0; t < DPL; ++t) acc[i][t] *= alpha;
+      for (int j = 0; j < kSimtKeys; ++j) {
+        const float pjj = __shfl_sync(0xffffffffu, pj, j);
+        const float* vr = vt + j * d;
+#pragma unroll
+        for (int t = 0; t < DPL; ++t) {
+          const int c = lane + 32 * t;
+          if (c < d) acc[i][t] = fmaf(pjj, vr[c], acc[i][t]);
+        }
+      }
+      m[i] = m_new;
+    }
+  }
+
+#pragma unroll
+  for (int i = 0; i < kRowsPerWarp; ++i) {
+    const int row = row_base + warp * kRowsPerWarp + i;
+    if (row >= N) continue;
+    const float inv_l = 1.f / l[i];
+#pragma unroll
+    for (int t = 0; t < DPL; ++t) {
+      const int c = lane + 32 * t;
+      if (c < d) o[(head + row) * d + c] = acc[i][t] * inv_l;
+    }
+    if (lane == 0) lse[head + row] = m[i] + logf(l[i]);
+  }
+}
+
+template <int DPL, bool CAUSAL>
+int launch_simt_impl(const float* q, const float* k, const float* v, float* o, float* lse, int BH, int N, int d,
+                     float scale, const LaunchCtx& ctx) {
+  const size_t smem = sizeof(float) * (static_cast<size_t>(kSimtRows) * d + static_cast<size_t>(kSimtKeys) * (d | 1) +
+                                       static_cast<size_t>(kSimtKeys) * d);
+  auto kernel = fa_fwd_simt_kernel<DPL, CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return static_cast<int>(e);
+  const dim3 grid((N + kSimtRows - 1) / kSimtRows, BH);
+  kernel<<<grid, kSimtWarps * 32, smem, ctx.stream>>>(q, k, v, o, lse, N, d, scale);
+  return static_cast<int>(cudaGetLastError());
+}
+
+template <bool CAUSAL>
+int launch_simt_dpl(const float* q, const float* k, const float* v, float* o, float* lse, int BH, int N, int d,
+                    float scale, const LaunchCtx& ctx) {
+  if (d <= 32) return launch_simt_impl<1, CAUSAL>(q, k, v, o, lse, BH, N, d, scale, ctx);
+  if (d <= 64) return launch_simt_impl<2, CAUSAL>(q, k, v, o, lse, BH, N, d, scale, ctx);
+  if (d <= 128) return launch_simt_impl<4, CAUSAL>(q, k, v, o, lse, BH, N, d, scale, ctx);
+  return launch_simt_impl<8, CAUSAL>(q, k, v, o, lse, BH, N, d, scale, ctx);
+}
+
+}  // namespace
+
+int launch_simt(bool causal, const float* q, const float* k, const float* v, float* o, float* lse, int BH, int N,
+                int d, float scale, const LaunchCtx& ctx) {
+  return causal ? launch_simt_dpl<true>(q, k, v, o, lse, BH, N, d, scale, ctx)
+                : launch_simt_dpl<false>(q, k, v, o, lse, BH, N, d, scale, ctx);
+}
+
+}  // namespace fa
