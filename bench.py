@@ -33,7 +33,6 @@ import statistics
 import subprocess
 import sys
 import tempfile
-import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -133,6 +132,23 @@ def aggregate_ranks(local_seconds: float, world: int, reduce_max=None) -> float:
     if world <= 1 or reduce_max is None:
         return local_seconds
     return reduce_max(local_seconds)
+
+
+def make_reduce_max(dist, device):
+    """All-reduce(MAX) of one float over the default process group."""
+    import torch
+
+    def reduce_max(x: float) -> float:
+        t = torch.tensor([x], device=device, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    return reduce_max
+
+
+def job_throughput(world: int, steps: int, flops_per_step: float, seconds: float) -> float:
+    """Whole-job TFLOP/s: every rank ran `steps` steps of `flops_per_step` in `seconds` (max over ranks)."""
+    return world * steps * flops_per_step / seconds / 1e12
 
 
 # ------------------------------------------------------------------ CPU oracle legs
@@ -240,11 +256,7 @@ def run_ours(args, w):
     reduce_max = None
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
-
-        def reduce_max(x):
-            t = torch.tensor([x], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            return float(t.item())
+        reduce_max = make_reduce_max(dist, dev)
 
     def barrier():
         if world > 1:
@@ -287,7 +299,7 @@ def run_ours(args, w):
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     local_s = sum(step_ms) / 1e3
     total_s = aggregate_ranks(local_s, world, reduce_max)
-    value = world * args.steps * w.flops / total_s / 1e12
+    value = job_throughput(world, args.steps, w.flops, total_s)
     kernel_ms = statistics.mean(step_ms)
 
     # End to end through the C ABI on HOST buffers: H2D of Q, K, V from pinned
@@ -318,7 +330,7 @@ def run_ours(args, w):
         barrier()
         e2e_s = aggregate_ranks(e0.elapsed_time(e1) / 1e3, world, reduce_max)
         tb = w.B * w.H * w.N * w.d * 2
-        e2e = {"value": world * args.steps * w.flops / e2e_s / 1e12, "unit": UNIT,
+        e2e = {"value": job_throughput(world, args.steps, w.flops, e2e_s), "unit": UNIT,
                "h2d_bytes_per_step": 3 * tb, "d2h_bytes_per_step": tb + w.B * w.H * w.N * 4,
                "ms_per_step": e2e_s / args.steps * 1e3, "api": "fa_fwd_host (C ABI, pinned host buffers)"}
         fa.check_status(dev)

@@ -64,8 +64,12 @@ struct TcCfg {
   static constexpr int NS_FIT = (SMEM_LIMIT - 2048 - NQT * Q_TILE) / KV_TILE;
   static constexpr int NS = NS_FIT > 8 ? 8 : NS_FIT;   // K/V ring slots
   static constexpr int NO = NQT;                       // O accumulators in TMEM
-  static constexpr int TM_S = 0;                       // S/P buffer b at columns b*BK
-  static constexpr int TM_O = 2 * BK;                  // O accumulator t at TM_O + t*D
+  // TMEM columns.  Every S/P buffer starts on a multiple of 128 columns and
+  // every O accumulator on a multiple of its own width: S/P buffer b at
+  // TM_S + b*128, O accumulator t at TM_O + t*D.
+  static constexpr int TM_S = (D == 256) ? 256 : 0;
+  static constexpr int TM_O = (D == 256) ? 0 : 256;
+  static constexpr int TM_SB = 128;                    // column stride of the S/P buffers
   static constexpr int TM_COLS = 512;
   static constexpr int SOFTMAX_WARPS = 4 * NQT;
   static constexpr int MMA_WARP = SOFTMAX_WARPS;
@@ -83,7 +87,8 @@ struct TcCfg {
   static constexpr int SMEM_ALLOC = SMEM_USED < 120 * 1024 ? 120 * 1024 : SMEM_USED;
   static_assert(D == 32 || D == 64 || D == 128 || D == 256, "head dim");
   static_assert(NS >= 2, "K/V ring");
-  static_assert(TM_O + NO * D <= TM_COLS, "TMEM budget");
+  static_assert((D == 256) ? (TM_S + 2 * TM_SB <= TM_COLS && NO * D <= TM_S)
+                           : (TM_O + NO * D <= TM_COLS && 2 * TM_SB <= TM_O), "TMEM budget");
   static_assert(SMEM_USED <= SMEM_LIMIT, "shared memory budget");
 };
 
@@ -254,7 +259,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
         return r;
       };
       auto issue_qk = [&](int qt, int buf, uint32_t kslot) {
-        const uint32_t d_t = tmem + C::TM_S + buf * C::BK;
+        const uint32_t d_t = tmem + C::TM_S + buf * C::TM_SB;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const int k0 = kk * 16;
@@ -269,7 +274,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
       };
       auto issue_pv = [&](int ot, int buf, uint32_t vslot, bool acc) {
         const uint32_t d_t = tmem + C::TM_O + ot * D;
-        const uint32_t a_t = tmem + C::TM_S + buf * C::BK;
+        const uint32_t a_t = tmem + C::TM_S + buf * C::TM_SB;
 #pragma unroll
         for (int kk = 0; kk < C::BK / 16; ++kk) {
           const uint64_t b = make_sdesc(base + C::OFF_KV + vslot * C::KV_TILE + kk * 16 * C::SWB, C::KV_REGION,
@@ -381,6 +386,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
       const int row = row0 + r;
       float m = -INFINITY;  // running max of scaled logits, log2 units
       float l = 0.f;        // running sum of exp2(x - m)
+      float lw = 0.f;       // the same sum over the bf16-rounded weights
       for (int j = 0; j < n; ++j) {
         const int buf = (C::NQT == 2) ? wg : static_cast<int>(s_waits & 1);
         const uint32_t par = (C::NQT == 2) ? (s_waits & 1) : ((s_waits >> 1) & 1);
@@ -389,7 +395,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
         if (!ok) break;
         ++s_waits;
         tc_fence_after();
-        const uint32_t ts = tmem + lane_off + C::TM_S + buf * C::BK;
+        const uint32_t ts = tmem + lane_off + C::TM_S + buf * C::TM_SB;
 
         float s[C::BK];
         {
@@ -424,19 +430,24 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
         const float m_new = grow ? m_cand : m;
         const float alpha = grow ? ex2(m - m_new) : 1.f;   // ex2(-inf) = 0 on the first tile
         const float nbase = (m_new == -INFINITY) ? 0.f : -m_new;
-        float sum[8];
+        // Two row sums: lsum of the fp32 weights (for L, the logsumexp) and
+        // wsum of the bf16-rounded weights that P V multiplies (for O / l, so
+        // the division normalises exactly the weights that were applied).
+        float lsum[4], wsum[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) sum[i] = 0.f;
+        for (int i = 0; i < 4; ++i) lsum[i] = wsum[i] = 0.f;
         uint32_t pk[C::BK / 2];
 #pragma unroll
         for (int c = 0; c < C::BK; c += 2) {
           const float p0 = ex2(fmaf(s[c], sl2, nbase));
           const float p1 = ex2(fmaf(s[c + 1], sl2, nbase));
-          sum[(c >> 1) & 7] += p0 + p1;
-          pk[c >> 1] = pack_bf16x2(p0, p1);
+          const uint32_t w = pack_bf16x2(p0, p1);
+          pk[c >> 1] = w;
+          lsum[(c >> 1) & 3] += p0 + p1;
+          wsum[(c >> 1) & 3] += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
         }
-        const float rsum = ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
-        l = l * alpha + rsum;
+        l = l * alpha + ((lsum[0] + lsum[1]) + (lsum[2] + lsum[3]));
+        lw = lw * alpha + ((wsum[0] + wsum[1]) + (wsum[2] + wsum[3]));
         m = m_new;
 #pragma unroll
         for (int c = 0; c < C::BK / 64; ++c) {
@@ -446,12 +457,18 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
           tmem_st32(ts + c * 32, chunk);
         }
         tmem_wait_st();
-        // Rescale the O accumulator of this row when its max grew past the threshold.
-        const bool need = grow && j > 0;
-        if (__any_sync(0xffffffffu, need)) {
+        if (j > 0) {
+          // Observe the completion of P V number j-1 on this accumulator.  Every
+          // completion of o_done is waited for in order: a parity wait that ran
+          // two phases ahead of the barrier would read an older phase as done.
+          // (At most P V j-1 can be outstanding: P V j needs this tile's P.)
           ok = wait_bar(o_done(ot), (pv_done + j - 1) & 1, g, kStatusTimeoutSoftmax);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
+        }
+        // Rescale the O accumulator of this row when its max grew past the threshold.
+        const bool need = grow && j > 0;
+        if (__any_sync(0xffffffffu, need)) {
           tc_fence_after();
           const uint32_t to = tmem + lane_off + C::TM_O + ot * D;
 #pragma unroll 1
@@ -470,12 +487,13 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
       }
       if (!ok) break;
       // ---- epilogue: O / l in bf16, L = (m + log2 l) * ln 2
+      // P V number n-1 is the only one not yet observed (see above).
       ok = wait_bar(o_done(ot), (pv_done + n - 1) & 1, g, kStatusTimeoutSoftmax);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       pv_done += n;
       tc_fence_after();
-      const float inv_l = 1.f / l;
+      const float inv_l = 1.f / lw;
       const uint32_t to = tmem + lane_off + C::TM_O + ot * D;
       __nv_bfloat16* orow = p.o + (static_cast<size_t>(w.bh) * p.N + row) * D;
 #pragma unroll 1
