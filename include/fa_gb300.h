@@ -53,7 +53,8 @@ enum {
   FA_ERR_TIMEOUT = -6,        /* a bounded device-side wait expired (reported by fa_status)  */
   FA_ERR_ARCH = -7,           /* the current device is not a compute capability 10.3 GPU     */
   FA_ERR_BAD_SCALE = -8,      /* scale is not a finite number > 0                            */
-  FA_ERR_WORKSPACE = -9       /* the workspace passed to fa_fwd_host is too small            */
+  FA_ERR_WORKSPACE = -9,      /* the workspace passed to fa_fwd_host is too small            */
+  FA_ERR_SCRATCH = -10        /* the kernel needs more scratch than fa_fwd_noalloc provides  */
 };
 
 /*
@@ -107,6 +108,42 @@ size_t fa_fwd_host_workspace_bytes(int B, int H, int N, int d);
 int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse,
                 void* workspace, size_t workspace_bytes,
                 int B, int H, int N, int d, float scale, int causal, void* stream);
+
+/*
+ * fa_fwd_noalloc - fa_fwd for callers that must not allocate device memory.
+ * (No counterpart in the pages: this entry point exists for deployment, not
+ * for the method.)
+ *
+ * Who needs it: code that is handed a stream and must not allocate while it
+ * runs - an operator or plug-in inside an inference runtime whose enqueue
+ * call may not allocate (an allocation can synchronise the device, and memory
+ * obtained while a stream is being captured cannot be relied on when the
+ * graph replays), a latency-critical serving path that cannot afford the
+ * implicit synchronisation and variable latency of cudaMalloc, or a process
+ * that reserves all device memory up front.  fa_fwd allocates a small status
+ * word on its first call on each device; this entry point never calls
+ * cudaMalloc, cudaFree or any allocating routine.
+ *
+ * Arguments, layout, supported d, asynchrony and return codes are those of
+ * fa_fwd (same kernel, same results).  The kernel's scratch - the status word
+ * of its bounded device-side waits, 4 bytes, independent of B, H, N and d -
+ * lives in a static device array of 256 bytes that every GPU which loads the
+ * library holds until the process exits; a kernel that needed more than that
+ * would be rejected with FA_ERR_SCRATCH before anything is enqueued.
+ *
+ * Each call first clears the status word with cudaMemsetAsync on `stream`,
+ * then launches.  All calls on a device share the one array: calls whose
+ * kernels overlap on the GPU (on different streams) race on it.  A wait that
+ * expires ends the kernel early as with fa_fwd, but is recorded only in this
+ * shared word, which fa_status() does not read.
+ *
+ * The first call on each device does the set-up (with that device current):
+ * it looks up the array's device address with cudaGetSymbolAddress, queries
+ * the device attributes and resolves the driver's tensor-map encoder.  Make
+ * that first call before any stream capture begins.
+ */
+int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                   int B, int H, int N, int d, float scale, int causal, void* stream);
 
 /*
  * fa_status - synchronises `stream`, then reads and clears the device status

@@ -6,10 +6,10 @@ only loads it and marshals arguments.  Build it with
 ``python -m tiled_attention_fwd_gb300.build``.
 """
 from ._lib import (FAError, check_status, declared_functions, fa_abi_version, fa_fwd, fa_fwd_f32,
-                   fa_fwd_host, fa_fwd_host_workspace_bytes, fa_set_wait_limit_ms, fa_status, fa_strerror,
+                   fa_fwd_host, fa_fwd_host_workspace_bytes, fa_fwd_noalloc, fa_set_wait_limit_ms, fa_status, fa_strerror,
                    forward, load)
 
 __all__ = [
     "FAError", "check_status", "declared_functions", "fa_abi_version", "fa_fwd", "fa_fwd_f32", "fa_fwd_host",
-    "fa_fwd_host_workspace_bytes", "fa_set_wait_limit_ms", "fa_status", "fa_strerror", "forward", "load",
+    "fa_fwd_host_workspace_bytes", "fa_fwd_noalloc", "fa_set_wait_limit_ms", "fa_status", "fa_strerror", "forward", "load",
 ]

@@ -24,6 +24,7 @@ _SIGNATURES = {
     "fa_fwd_f32": (_c_int, [_c_void_p] * 5 + [_c_int] * 4 + [_c_float, _c_int, _c_void_p]),
     "fa_fwd_host_workspace_bytes": (_c_size_t, [_c_int] * 4),
     "fa_fwd_host": (_c_int, [_c_void_p] * 6 + [_c_size_t] + [_c_int] * 4 + [_c_float, _c_int, _c_void_p]),
+    "fa_fwd_noalloc": (_c_int, [_c_void_p] * 5 + [_c_int] * 4 + [_c_float, _c_int, _c_void_p]),
     "fa_status": (_c_int, [_c_void_p]),
     "fa_set_wait_limit_ms": (_c_int, [_c_int]),
     "fa_strerror": (ctypes.c_char_p, [_c_int]),
@@ -97,6 +98,11 @@ def fa_fwd_host(q, k, v, o, lse, workspace, workspace_bytes, B, H, N, d, scale, 
     """bf16 forward on host buffers (copies in, kernel, copies out, all on `stream`)."""
     return load().fa_fwd_host(q, k, v, o, lse, workspace, workspace_bytes, B, H, N, d, scale,
                               int(bool(causal)), stream)
+
+
+def fa_fwd_noalloc(q, k, v, o, lse, B, H, N, d, scale, causal, stream) -> int:
+    """fa_fwd without any device allocation (scratch in a static device array)."""
+    return load().fa_fwd_noalloc(q, k, v, o, lse, B, H, N, d, scale, int(bool(causal)), stream)
 
 
 def fa_status(stream) -> int:

@@ -101,6 +101,23 @@ int encode_bf16_map(CUtensorMap* map, const void* ptr, int BH, int N, int D, int
   return r == CUDA_SUCCESS ? 0 : -1;
 }
 
+// Resolve cuTensorMapEncodeTiled without creating any per-device state
+// (used by the entry point that allocates nothing).  Returns 0 on success.
+int load_tensor_map_encoder() {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_encode != nullptr) return 0;
+  cudaDriverEntryPointQueryResult q;
+  void* fn = nullptr;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || fn == nullptr)
+    return -1;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return 0;
+}
+
+// Current time limit of the device-side waits, in nanoseconds.
+unsigned long long wait_limit_ns() { return static_cast<unsigned long long>(g_wait_limit_ms.load()) * 1000000ull; }
+
 }  // namespace fa
 
 extern "C" {
@@ -215,6 +232,7 @@ const char* fa_strerror(int code) {
     case FA_ERR_ARCH: return "FA_ERR_ARCH: the current device is not compute capability 10.3";
     case FA_ERR_BAD_SCALE: return "FA_ERR_BAD_SCALE: scale must be finite and > 0";
     case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE: workspace too small";
+    case FA_ERR_SCRATCH: return "FA_ERR_SCRATCH: the kernel needs more scratch than fa_fwd_noalloc's static array holds";
     default: return "unknown fa_gb300 error code";
   }
 }

@@ -24,6 +24,12 @@ struct LaunchCtx {
 int encode_bf16_map(CUtensorMap* map, const void* ptr, int BH, int N, int D, int box_cols, int box_rows,
                     int swizzle_bytes);
 
+// Resolve the driver's tensor-map encoder (no device state, no allocation).  Returns 0 on success.
+int load_tensor_map_encoder();
+
+// Current time limit of the device-side waits (fa_set_wait_limit_ms), in nanoseconds.
+unsigned long long wait_limit_ns();
+
 // bf16 tensor-core forward for one head dimension; returns a cudaError_t-like
 // code (0 = launched).  Defined in fa_tc_d<D>.cu.
 int launch_tc_d32(bool causal, const void* q, const void* k, const void* v, void* o, float* lse, int BH, int N,

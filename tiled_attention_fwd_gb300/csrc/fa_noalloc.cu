@@ -1,0 +1,100 @@
+// fa_fwd_noalloc: the bf16 tensor-core forward pass for callers that cannot
+// allocate device memory (see include/fa_gb300.h).  The only device memory
+// the kernel needs besides its inputs and outputs is a small scratch area
+// (the status word of its bounded waits); here it lives in a file-scope
+// static __device__ array instead of memory the library allocates.
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/fa_gb300.h"
+#include "fa_internal.h"
+
+namespace fa {
+namespace {
+
+// Scratch of the allocation-free entry point: 64 words (256 bytes) per device,
+// part of the module image, so every GPU that loads the library holds it until
+// exit.  Word 0 is the status word of the kernel's bounded waits.
+constexpr int kNoAllocScratchWords = 64;
+__device__ __align__(256) int g_noalloc_scratch[kNoAllocScratchWords];
+
+// Scratch words one launch of the tensor-core kernel uses (the status word).
+// It does not depend on B, H, N or d.
+constexpr int kTcScratchWords = 1;
+
+constexpr int kMaxDevices = 64;
+
+struct NoAllocDevice {
+  bool ready = false;
+  int* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+  int num_sms = 0;
+};
+
+std::mutex g_na_mutex;
+NoAllocDevice g_na_devices[kMaxDevices];
+
+// Once per device, with that device current: look up the device address of
+// the scratch array (the host-side symbol is only a stand-in, not a device
+// address), the SM count, and the tensor-map encoder.  Allocates nothing.
+int noalloc_device(NoAllocDevice** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_na_mutex);
+  NoAllocDevice& s = g_na_devices[dev];
+  if (!s.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return FA_ERR_CUDA;
+    if (major != 10 || minor != 3) return FA_ERR_ARCH;
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return FA_ERR_CUDA;
+    if (load_tensor_map_encoder() != 0) return FA_ERR_CUDA;
+    s.scratch = static_cast<int*>(ptr);
+    s.num_sms = sms;
+    s.ready = true;
+  }
+  *out = &s;
+  return FA_OK;
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                              int N, int d, float scale, int causal, void* stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_NULL_POINTER;
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_BAD_SHAPE;
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh > 0x7fffffffLL || bh * ((static_cast<long long>(N) + 255) / 256) > 0x7fffffffLL) return FA_ERR_BAD_SHAPE;
+  if (static_cast<long long>(N) * 256 * 2 >= (1LL << 40)) return FA_ERR_BAD_SHAPE;
+  if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_BAD_SCALE;
+  if (d != 32 && d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED_D;
+  const uintptr_t a16 = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o);
+  if ((a16 & 15u) || (reinterpret_cast<uintptr_t>(lse) & 3u)) return FA_ERR_MISALIGNED;
+  if (fa::kTcScratchWords > fa::kNoAllocScratchWords) return FA_ERR_SCRATCH;
+  fa::NoAllocDevice* s = nullptr;
+  int rc = fa::noalloc_device(&s);
+  if (rc != FA_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // The status word must start at zero for this call; the array keeps whatever the previous call left.
+  if (cudaMemsetAsync(s->scratch, 0, sizeof(int) * fa::kTcScratchWords, st) != cudaSuccess) return FA_ERR_CUDA;
+  fa::LaunchCtx ctx;
+  ctx.status = s->scratch;
+  ctx.limit_ns = fa::wait_limit_ns();
+  ctx.num_sms = s->num_sms;
+  ctx.stream = st;
+  const int BH = B * H;
+  const bool c = causal != 0;
+  int e = 0;
+  switch (d) {
+    case 32: e = fa::launch_tc_d32(c, q, k, v, o, lse, BH, N, scale, ctx); break;
+    case 64: e = fa::launch_tc_d64(c, q, k, v, o, lse, BH, N, scale, ctx); break;
+    case 128: e = fa::launch_tc_d128(c, q, k, v, o, lse, BH, N, scale, ctx); break;
+    default: e = fa::launch_tc_d256(c, q, k, v, o, lse, BH, N, scale, ctx); break;
+  }
+  return e == 0 ? FA_OK : FA_ERR_CUDA;
+}
