@@ -15,7 +15,7 @@ import numpy as np
 import torch
 
 import oracle
-from tiled_attention_fwd_gb300 import forward
+from tiled_attention_fwd_gb300 import check_status, forward
 from tiled_attention_fwd_gb300.inputs import Workload, as_f64_numpy, make_qkv
 
 TOL_F32 = 1e-5
@@ -33,7 +33,7 @@ def run_cuda(q, k, v, causal, scale, poison=True):
         o.fill_(float("nan"))
         lse.fill_(float("nan"))
     forward(qd, kd, vd, causal=causal, scale=scale, out=o, lse=lse)
-    torch.cuda.synchronize()
+    check_status(dev)  # synchronises; raises if any bounded device wait of this launch expired
     return as_f64_numpy(o.cpu()), lse.cpu().double().numpy()
 
 

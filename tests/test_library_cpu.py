@@ -98,3 +98,20 @@ def test_missing_library_fails_loudly(tmp_path):
             _lib.load(str(tmp_path / "nope.so"))
     finally:
         _lib._lib = saved
+
+
+def test_tensor_core_kernels_fit_their_register_split():
+    """The d <= 128 kernels launch 512 threads at 128 registers and re-split them
+    (176 x 256 softmax + 72 x 128 correction + 88 x 128 MMA/TMA = 65536); any
+    other launch count would stall setmaxnreg, and none of them may spill."""
+    if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+        pytest.skip("nvcc not available")
+    rep = build.ptxas_report({"fa_tc_d32.cu", "fa_tc_d64.cu", "fa_tc_d128.cu", "fa_tc_d256.cu"})
+    tc = {k: v for k, v in rep.items() if "fa_fwd_tc_kernel" in k}
+    assert len(tc) == 8
+    for name, r in tc.items():
+        assert r["spill_stores"] == 0 and r["spill_loads"] == 0, (name, r)
+        if "ILi256E" not in name:
+            assert r["registers"] == 128, (name, r)
+        else:
+            assert r["registers"] <= 168, (name, r)

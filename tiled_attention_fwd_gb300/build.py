@@ -88,6 +88,41 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     return LIB
 
 
+def ptxas_report(names=None):
+    """Compile translation units with -Xptxas -v (objects discarded) and return
+    {kernel_name: {"registers": int, "spill_stores": int, "spill_loads": int}}."""
+    import re
+    import tempfile
+
+    nvcc = nvcc_path()
+    srcs = [s for s in sources() if names is None or os.path.basename(s) in names]
+    out = {}
+
+    def one(src):
+        with tempfile.TemporaryDirectory() as td:
+            cmd = [nvcc, *NVCC_FLAGS, "-Xptxas", "-v", "-I", INCLUDE, "-c", src, "-o", os.path.join(td, "x.o")]
+            return subprocess.run(cmd, capture_output=True, text=True)
+
+    with concurrent.futures.ThreadPoolExecutor(max_workers=len(srcs) or 1) as ex:
+        for r in ex.map(one, srcs):
+            if r.returncode != 0:
+                raise RuntimeError(r.stderr)
+            cur = None
+            for line in r.stderr.splitlines():
+                m = re.search(r"Compiling entry function '([^']+)'", line)
+                if m:
+                    cur = m.group(1)
+                    out[cur] = {}
+                m = re.search(r"(\d+) bytes spill stores, (\d+) bytes spill loads", line)
+                if m and cur:
+                    out[cur]["spill_stores"] = int(m.group(1))
+                    out[cur]["spill_loads"] = int(m.group(2))
+                m = re.search(r"Used (\d+) registers", line)
+                if m and cur:
+                    out[cur]["registers"] = int(m.group(1))
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--force", action="store_true")

@@ -6,25 +6,37 @@
 // masking"): for each 128-row query tile Q_i, loop over key/value tiles
 // K_j, V_j; S = Q_i K_j^T; fold S into the running row max m, the rescaled row
 // sum l and the unnormalised output O (rescale factor exp(m_old - m_new));
-// divide by l once at the end and store L = m + log l.
+// divide by l once at the end and store L = m + log l.  The rescale of O is
+// skipped for rows whose max did not grow (the guarded correction of "Case
+// Study: metal-flash-attention").
 //
-// Mapping onto one GB300 SM (one persistent CTA per SM):
-//   * a TMA producer warp streams Q tiles and a ring of NS K/V tiles into
-//     128-byte-swizzled shared memory, each slot guarded by full/empty mbarriers;
-//   * one MMA warp issues tcgen05.mma: S = Q K^T into tensor memory (TMEM),
-//     then O += P V with P read from TMEM and V from shared memory;
-//   * softmax warpgroups (one thread per query row = one TMEM lane) read S with
-//     tcgen05.ld, apply mask and scale, update m and l, write P as bf16 back
-//     into the S columns with tcgen05.st, and rescale O in TMEM when the row
-//     max moved by more than a factor 2^8 (the guarded correction of the
-//     metal-flash-attention case study, with a threshold);
-//   * for d <= 128 a work unit is two query tiles (256 rows) sharing every
-//     K/V tile, and the MMA warp alternates between them so that one tile's
-//     softmax overlaps the other tile's matrix products (ping-pong);
-//     for d = 256 a work unit is one query tile and S is double-buffered;
-//   * work units (batch*head, query block) are ordered heaviest first for the
-//     causal mask and strided over the persistent CTAs; key tiles wholly in the
-//     future of a query tile are never loaded or multiplied.
+// Mapping onto one GB300 SM (one persistent CTA per SM), by warpgroup:
+//   * softmax warpgroup(s), one per 128-row query tile (thread = row = TMEM
+//     lane): read S from tensor memory (TMEM), mask, row max, publish the
+//     rescale factor alpha, P = exp2(S*scale*log2e - m) with paired fp32
+//     arithmetic, write P as bf16 over S in TMEM, keep m and l;
+//   * a correction warpgroup: rescales the O accumulators in TMEM by alpha
+//     while the softmax computes P, and runs the epilogue (O / l in bf16,
+//     L = m + log l) so the softmax can start the next work unit at once;
+//   * one MMA warp: tcgen05.mma S = Q K^T into TMEM, then O += P V with P read
+//     from TMEM and V from shared memory;
+//   * one TMA producer warp: Q tiles and a ring of K/V stages in 128-byte
+//     swizzled shared memory, each stage guarded by full/empty mbarriers.
+// For d <= 128 a work unit is two query tiles (256 rows) that share every K/V
+// tile, and the MMA warp alternates between them so one tile's softmax
+// overlaps the other tile's matrix products; for d = 256 a work unit is one
+// query tile with a double-buffered S.  Work units (batch*head, query block)
+// are ordered heaviest first for the causal mask and strided over the
+// persistent CTAs; key tiles wholly in the future of a query tile are never
+// loaded or multiplied.
+//
+// The tensor core executes MMAs about as fast as one thread can issue them,
+// so the MMA warp is kept lean: one readiness barrier per P V product (the
+// softmax's P and the correction's O meet there), one barrier per K/V stage,
+// descriptors built once.
+//
+// Every mbarrier phase is waited for in order by its consumer: a parity wait
+// issued two phases ahead of a barrier would read an older phase as complete.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -51,7 +63,7 @@ struct TcCfg {
   static constexpr int BQ = 128;                       // query rows per tile (= TMEM lanes)
   static constexpr int NQT = (D <= 128) ? 2 : 1;       // query tiles per work unit
   static constexpr int BK = (D <= 128) ? 128 : 64;     // keys per K/V tile
-  static constexpr int LA = (NQT == 1) ? 2 : 1;        // K tiles ahead of V in the ring order
+  static constexpr int LA = (NQT == 1) ? 2 : 1;        // K tiles needed before the first P V
   static constexpr int SWB = (D * 2 >= 128) ? 128 : D * 2;  // swizzle span in bytes
   static constexpr uint32_t SWZ = (SWB == 128) ? 2u : 4u;   // descriptor swizzle code
   static constexpr int RC = SWB / 2;                   // bf16 columns per swizzle region
@@ -60,33 +72,49 @@ struct TcCfg {
   static constexpr int KV_REGION = BK * SWB;
   static constexpr int Q_TILE = BQ * D * 2;
   static constexpr int KV_TILE = BK * D * 2;
-  static constexpr int SMEM_LIMIT = 227 * 1024;
-  static constexpr int NS_FIT = (SMEM_LIMIT - 2048 - NQT * Q_TILE) / KV_TILE;
-  static constexpr int NS = NS_FIT > 8 ? 8 : NS_FIT;   // K/V ring slots
   static constexpr int NO = NQT;                       // O accumulators in TMEM
-  // TMEM columns.  Every S/P buffer starts on a multiple of 128 columns and
-  // every O accumulator on a multiple of its own width: S/P buffer b at
-  // TM_S + b*128, O accumulator t at TM_O + t*D.
-  static constexpr int TM_S = (D == 256) ? 256 : 0;
-  static constexpr int TM_O = (D == 256) ? 0 : 256;
-  static constexpr int TM_SB = 128;                    // column stride of the S/P buffers
-  static constexpr int TM_COLS = 512;
-  static constexpr int SOFTMAX_WARPS = 4 * NQT;
-  static constexpr int MMA_WARP = SOFTMAX_WARPS;
-  static constexpr int LOAD_WARP = SOFTMAX_WARPS + 1;
-  static constexpr int THREADS = 32 * (SOFTMAX_WARPS + 2);
+  // Shared memory: [Q tiles][K/V stages][misc]; misc = barriers, alpha, m/l, TMEM address, abort flag.
+  static constexpr int MISC = 6144;
+  static constexpr int SMEM_LIMIT = 227 * 1024;
+  // A K/V stage holds two tiles: V_j and K_{j+LA} (the first stage of a unit: K_0 .. K_{LA-1}).
+  static constexpr int STAGE = 2 * KV_TILE;
+  static constexpr int NST_FIT = (SMEM_LIMIT - 1024 - MISC - NQT * Q_TILE) / STAGE;
+  static constexpr int NST = NST_FIT > 4 ? 4 : NST_FIT;  // K/V stages
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = NQT * Q_TILE;
-  static constexpr int OFF_BAR = OFF_KV + NS * KV_TILE;
-  // barriers: q_full, q_empty, kv_full[NS], kv_empty[NS], s_full[2], p_full[2],
-  // o_done[NO], o_free[NO], drain
-  static constexpr int NBAR = 2 + 2 * NS + 4 + 2 * NO + 1;
-  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // TMEM base address, abort flag
-  static constexpr int SMEM_USED = OFF_MISC + 16 + 1024;  // + slack for 1024-byte alignment
+  static constexpr int OFF_MISC = OFF_KV + NST * STAGE;
+  static constexpr int OFF_BAR = OFF_MISC;                    // 64 barriers at most
+  static constexpr int OFF_ALPHA = OFF_MISC + 512;            // float [NO][2][128] (by step parity)
+  static constexpr int OFF_STAT_M = OFF_ALPHA + 4 * 128 * 4;  // float [NO][128]
+  static constexpr int OFF_STAT_L = OFF_STAT_M + 2 * 128 * 4; // float [NO][128]
+  static constexpr int OFF_TMEM_SLOT = OFF_STAT_L + 2 * 128 * 4;
+  static constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
+  static constexpr int SMEM_USED = OFF_MISC + MISC + 1024;    // + slack for 1024-byte alignment
   // At least ~120 KB so that a second CTA never shares the SM (and its TMEM).
   static constexpr int SMEM_ALLOC = SMEM_USED < 120 * 1024 ? 120 * 1024 : SMEM_USED;
+  // TMEM columns.  S/P buffer b at TM_S + b*128, O accumulator t at TM_O + t*D.
+  static constexpr int TM_S = (D == 256) ? 256 : 0;
+  static constexpr int TM_O = (D == 256) ? 0 : 256;
+  static constexpr int TM_SB = 128;
+  static constexpr int TM_COLS = 512;
+  // Warp roles.
+  static constexpr int SOFTMAX_WARPS = 4 * NQT;
+  static constexpr int CORR_WARP0 = SOFTMAX_WARPS;       // four warps
+  static constexpr int MMA_WARP = SOFTMAX_WARPS + 4;
+  static constexpr int LOAD_WARP = MMA_WARP + 1;
+  static constexpr int THREADS = 32 * (SOFTMAX_WARPS + 8);  // + correction WG + MMA/TMA WG
+  // Register split (d <= 128, 512 threads launched at 128 registers each):
+  // softmax 176, correction 72, MMA/TMA warpgroup 88; 2*128*176 + 128*72 + 128*88 = 65536.
+  static constexpr bool SPLIT_REGS = (NQT == 2);
+  static constexpr uint32_t REG_SOFTMAX = 176;
+  static constexpr uint32_t REG_CORR = 72;
+  static constexpr uint32_t REG_OTHER = 88;
+  static constexpr int LAUNCH_REGS = 65536 / THREADS > 255 ? 255 : (65536 / THREADS) & ~7;
+  static_assert(!SPLIT_REGS || 2 * 128 * REG_SOFTMAX + 128 * REG_CORR + 128 * REG_OTHER <= THREADS * LAUNCH_REGS,
+                "register split exceeds the launch budget");
   static_assert(D == 32 || D == 64 || D == 128 || D == 256, "head dim");
-  static_assert(NS >= 2, "K/V ring");
+  static_assert(NST >= 2, "K/V stages");
+  static_assert(LA <= 2, "a stage holds at most two K tiles");
   static_assert((D == 256) ? (TM_S + 2 * TM_SB <= TM_COLS && NO * D <= TM_S)
                            : (TM_O + NO * D <= TM_COLS && 2 * TM_SB <= TM_O), "TMEM budget");
   static_assert(SMEM_USED <= SMEM_LIMIT, "shared memory budget");
@@ -137,6 +165,473 @@ __device__ __forceinline__ bool wait_bar_drain(uint32_t bar, uint32_t parity, co
   return true;
 }
 
+// Barrier addresses in shared memory.
+template <int D>
+struct TcBars {
+  using C = TcCfg<D>;
+  uint32_t b0;
+  __device__ __forceinline__ uint32_t q_full() const { return b0; }
+  __device__ __forceinline__ uint32_t q_empty() const { return b0 + 8; }
+  __device__ __forceinline__ uint32_t kv_full(int i) const { return b0 + 16 + 8u * i; }
+  __device__ __forceinline__ uint32_t kv_empty(int i) const { return b0 + 16 + 8u * (C::NST + i); }
+  __device__ __forceinline__ uint32_t s_full(int b) const { return b0 + 16 + 8u * (2 * C::NST + b); }
+  // P V number g into accumulator t may start: P written (4 softmax warps) and
+  // O ready (4 correction warps: rescaled, or released by the previous
+  // epilogue).  Two-tile mode: barrier (t, 0).  Single-tile mode: barrier
+  // (0, g & 1), each completing once per two P V products, because there S of
+  // step j+1 is computed before P V j and the softmax may post P j+1 while
+  // P V j still waits for the correction warpgroup.
+  __device__ __forceinline__ uint32_t pv_go(int t, int k) const { return b0 + 16 + 8u * (2 * C::NST + 2 + 2 * t + k); }
+  // alpha of rescale step k of accumulator t published: barrier (t, k & 1), each
+  // completing once per two steps (single-tile mode lets the softmax run two
+  // steps ahead of the correction warpgroup).
+  __device__ __forceinline__ uint32_t a_full(int t, int k) const { return b0 + 16 + 8u * (2 * C::NST + 6 + 2 * t + k); }
+  __device__ __forceinline__ uint32_t o_done(int t) const { return b0 + 16 + 8u * (2 * C::NST + 10 + t); }
+  __device__ __forceinline__ uint32_t l_full(int t) const { return b0 + 16 + 8u * (2 * C::NST + 12 + t); }
+  __device__ __forceinline__ uint32_t drain() const { return b0 + 16 + 8u * (2 * C::NST + 14); }
+  static constexpr int COUNT = 2 + 2 * C::NST + 15;
+  static_assert(COUNT * 8 <= 512, "barrier area");
+};
+
+// ------------------------------------------------------------------ TMA producer
+// Run by one thread (lane 0 of the producer warp).
+// Stage sequence of a unit: {K_0 .. K_{LA-1}}, then {V_j, K_{j+LA}} for j < nmax.
+template <int D, bool CAUSAL>
+__device__ __forceinline__ void tc_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                                            const TcParams& p, const TcBars<D>& bar, uint32_t base,
+                                            const WaitGuard& g) {
+  using C = TcCfg<D>;
+  const uint64_t pol_q = policy_evict_first();
+  const uint64_t pol_kv = policy_evict_last();
+  uint32_t pos = 0;       // stages issued so far
+  uint32_t issued = 0;    // bit i: stage i has been loaded at least once
+  uint32_t last_par = 0;  // bit i: parity of stage i's latest load
+  int ui = 0;             // units started by this CTA
+  int last_q = -1;        // unit index of the latest Q load
+  bool ok = true;
+  auto load_tile = [&](const CUtensorMap* tm, uint32_t dst, uint32_t full, int j, int bh) {
+    for (int r = 0; r < C::NR; ++r) tma_load_3d(dst + r * C::KV_REGION, tm, full, r * C::RC, j * C::BK, bh, pol_kv);
+  };
+  for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x, ++ui) {
+    const TcUnit w = tc_decode<D, CAUSAL>(u, p);
+    if (!wait_bar(bar.q_empty(), (ui & 1) ^ 1, g, kStatusTimeoutLoad)) {
+      ok = false;
+      break;
+    }
+    mbar_arrive_expect_tx(bar.q_full(), C::NQT * C::Q_TILE);
+    for (int s = 0; s < C::NQT; ++s)
+      for (int r = 0; r < C::NR; ++r)
+        tma_load_3d(base + C::OFF_Q + s * C::Q_TILE + r * C::Q_REGION, tm_q, bar.q_full(), r * C::RC,
+                    w.row0 + s * C::BQ, w.bh, pol_q);
+    last_q = ui;
+    for (int t = -1; ok && t < w.nmax; ++t) {
+      const int st = pos % C::NST;
+      const uint32_t par = (pos / C::NST) & 1;
+      if (!wait_bar(bar.kv_empty(st), par ^ 1, g, kStatusTimeoutLoad)) {
+        ok = false;
+        break;
+      }
+      const uint32_t s0 = base + C::OFF_KV + st * C::STAGE;
+      if (t < 0) {  // K_0 .. K_{LA-1}
+        const int nk = C::LA < w.nmax ? C::LA : w.nmax;
+        mbar_arrive_expect_tx(bar.kv_full(st), nk * C::KV_TILE);
+        for (int k = 0; k < nk; ++k) load_tile(tm_k, s0 + k * C::KV_TILE, bar.kv_full(st), k, w.bh);
+      } else {  // V_t, K_{t+LA}
+        const bool has_k = t + C::LA < w.nmax;
+        mbar_arrive_expect_tx(bar.kv_full(st), (has_k ? 2 : 1) * C::KV_TILE);
+        load_tile(tm_v, s0, bar.kv_full(st), t, w.bh);
+        if (has_k) load_tile(tm_k, s0 + C::KV_TILE, bar.kv_full(st), t + C::LA, w.bh);
+      }
+      issued |= 1u << st;
+      last_par = (last_par & ~(1u << st)) | (par << st);
+      ++pos;
+    }
+  }
+  // Every issued copy must land before the CTA may exit.
+  for (int i = 0; i < C::NST; ++i)
+    if (issued & (1u << i)) wait_bar_drain(bar.kv_full(i), (last_par >> i) & 1, g);
+  if (last_q >= 0) wait_bar_drain(bar.q_full(), last_q & 1, g);
+}
+
+// ------------------------------------------------------------------ MMA issuer
+// Run by one thread (lane 0 of the MMA warp): under load from the softmax
+// warps sharing its scheduler, a lone thread issues tcgen05.mma at the tensor
+// core's rate, while a warp that re-converges around each group of MMAs does
+// not.  Descriptors are built once: a tile position or K step only adds a
+// constant to the address field (bits 0..13 hold address / 16, and no shared
+// address reaches 2^18).
+template <int D>
+struct TcMma {
+  using C = TcCfg<D>;
+  static constexpr uint32_t IDESC_QK = make_idesc_bf16(128, C::BK, 0);
+  static constexpr uint32_t IDESC_PV = make_idesc_bf16(128, D, 1);
+  // Address-field increments (16-byte units).
+  static constexpr __host__ __device__ uint32_t q_step(int kk) {
+    return ((kk * 16 / C::RC) * C::Q_REGION + (kk * 16 % C::RC) * 2) >> 4;
+  }
+  static constexpr __host__ __device__ uint32_t k_step(int kk) {
+    return ((kk * 16 / C::RC) * C::KV_REGION + (kk * 16 % C::RC) * 2) >> 4;
+  }
+  static constexpr __host__ __device__ uint32_t v_step(int kk) { return (kk * 16 * C::SWB) >> 4; }
+  static constexpr uint32_t TILE_STEP = C::KV_TILE >> 4;
+  static constexpr uint32_t QTILE_STEP = C::Q_TILE >> 4;
+
+  uint32_t tmem;
+  uint64_t dq0;   // Q tile 0, K-major
+  uint64_t dk0;   // K/V tile position 0, K-major (K as the B operand of S = Q K^T)
+  uint64_t dv0;   // K/V tile position 0, MN-major (V as the B operand of O = P V)
+
+  __device__ __forceinline__ TcMma(uint32_t tmem_, uint32_t base) : tmem(tmem_) {
+    dq0 = make_sdesc(base + C::OFF_Q, 16, 8 * C::SWB, C::SWZ);
+    dk0 = make_sdesc(base + C::OFF_KV, 16, 8 * C::SWB, C::SWZ);
+    dv0 = make_sdesc(base + C::OFF_KV, C::KV_REGION, 8 * C::SWB, C::SWZ);
+  }
+  // S[buf] = Q[qt] K^T with K at tile position kpos; completion on s_full_bar.
+  __device__ __forceinline__ void qk(int qt, int buf, uint32_t kpos, uint32_t s_full_bar) const {
+    const uint32_t d_t = tmem + C::TM_S + buf * C::TM_SB;
+    const uint64_t a = dq0 + qt * QTILE_STEP;
+    const uint64_t b = dk0 + kpos * TILE_STEP;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) mma_ss(d_t, a + q_step(kk), b + k_step(kk), IDESC_QK, kk > 0 ? 1u : 0u);
+    mma_commit(s_full_bar);
+  }
+  // O[ot] (+)= P[buf] V with V at tile position vpos.
+  __device__ __forceinline__ void pv(int ot, int buf, uint32_t vpos, bool acc) const {
+    const uint32_t d_t = tmem + C::TM_O + ot * D;
+    const uint32_t a_t = tmem + C::TM_S + buf * C::TM_SB;
+    const uint64_t b = dv0 + vpos * TILE_STEP;
+#pragma unroll
+    for (int kk = 0; kk < C::BK / 16; ++kk) mma_ts(d_t, a_t + kk * 8, b + v_step(kk), IDESC_PV, (acc || kk > 0) ? 1u : 0u);
+  }
+  __device__ __forceinline__ void commit(uint32_t bar) const { mma_commit(bar); }
+};
+
+template <int D, bool CAUSAL>
+__device__ __forceinline__ void tc_mma(const TcParams& p, const TcBars<D>& bar, uint32_t base, uint32_t tmem,
+                                       const WaitGuard& g) {
+  using C = TcCfg<D>;
+  const TcMma<D> M(tmem, base);
+  // Single-thread wait: a non-blocking test first, then the bounded wait.
+  auto wait = [&](uint32_t b, uint32_t par) -> bool {
+    return mbar_test_wait(b, par) || wait_bar(b, par, g, kStatusTimeoutMma);
+  };
+  uint32_t pos = 0;               // K/V stages consumed
+  uint32_t go0 = 0, go1 = 0;      // pv_go phases consumed, per O accumulator
+  uint32_t qk_total = 0;          // single-tile mode: S products issued so far
+  bool ok = true;
+  int ui = 0;
+
+  // Acquire the next K/V stage; its tiles sit at positions 2*st and 2*st + 1.
+  auto stage_acquire = [&](uint32_t& st) -> bool {
+    st = pos % C::NST;
+    const bool r = wait(bar.kv_full(st), (pos / C::NST) & 1);
+    ++pos;
+    return r;
+  };
+  auto pv_wait = [&](int t, uint32_t& go) -> bool {
+    const bool r = (C::NQT == 2) ? wait(bar.pv_go(t, 0), go & 1) : wait(bar.pv_go(0, go & 1), (go >> 1) & 1);
+    if (!r) return false;
+    ++go;
+    tc_fence_after();
+    return true;
+  };
+
+  for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x, ++ui) {
+    const TcUnit w = tc_decode<D, CAUSAL>(u, p);
+    if (!wait(bar.q_full(), ui & 1)) {
+      ok = false;
+      break;
+    }
+    uint32_t st;
+    if (!(ok = stage_acquire(st))) break;
+    tc_fence_after();
+    if constexpr (C::NQT == 2) {
+      // First stage: K_0.
+      if (w.n[0] > 0) M.qk(0, 0, 2 * st, bar.s_full(0));
+      if (w.n[1] > 0) M.qk(1, 1, 2 * st, bar.s_full(1));
+      M.commit(bar.kv_empty(st));
+      if (w.nmax == 1) M.commit(bar.q_empty());
+      for (int j = 0; j < w.nmax; ++j) {
+        // Stage j: V_j at position 2*st, K_{j+1} at 2*st + 1.
+        if (!(ok = stage_acquire(st))) break;
+        // query tile 0: P V j, then S for key tile j+1
+        if (j < w.n[0]) {
+          if (!(ok = pv_wait(0, go0))) break;
+          M.pv(0, 0, 2 * st, j > 0);
+          if (j == w.n[0] - 1) M.commit(bar.o_done(0));
+        }
+        if (j + 1 < w.n[0]) M.qk(0, 0, 2 * st + 1, bar.s_full(0));
+        // query tile 1
+        if (j < w.n[1]) {
+          if (!(ok = pv_wait(1, go1))) break;
+          M.pv(1, 1, 2 * st, j > 0);
+          if (j == w.n[1] - 1) M.commit(bar.o_done(1));
+        }
+        if (j + 1 < w.n[1]) M.qk(1, 1, 2 * st + 1, bar.s_full(1));
+        M.commit(bar.kv_empty(st));
+        if (j + 1 == w.nmax - 1) M.commit(bar.q_empty());
+      }
+    } else {
+      const int n = w.n[0];
+      const uint32_t qk_base = qk_total;  // S product of key tile j sits in buffer (qk_base + j) & 1
+      // First stage: K_0, K_1.
+      for (int t = 0; t < C::LA && t < n; ++t) {
+        M.qk(0, qk_total & 1, 2 * st + t, bar.s_full(qk_total & 1));
+        ++qk_total;
+      }
+      M.commit(bar.kv_empty(st));
+      if (n <= C::LA) M.commit(bar.q_empty());
+      for (int j = 0; j < n; ++j) {
+        // Stage j: V_j at 2*st, K_{j+2} at 2*st + 1.
+        if (!(ok = stage_acquire(st))) break;
+        if (!(ok = pv_wait(0, go0))) break;
+        M.pv(0, (qk_base + j) & 1, 2 * st, j > 0);
+        M.commit(bar.o_done(0));
+        if (j + C::LA < n) {
+          M.qk(0, qk_total & 1, 2 * st + 1, bar.s_full(qk_total & 1));
+          ++qk_total;
+          if (j + C::LA == n - 1) M.commit(bar.q_empty());
+        }
+        M.commit(bar.kv_empty(st));
+      }
+    }
+  }
+  (void)go1;
+  // All issued MMAs must complete before TMEM is released.
+  M.commit(bar.drain());
+  wait_bar_drain(bar.drain(), 0, g);
+}
+
+// ------------------------------------------------------------------ softmax
+template <int D, bool CAUSAL>
+__device__ __forceinline__ void tc_softmax(const TcParams& p, const TcBars<D>& bar, uint8_t* gbase, uint32_t tmem,
+                                           int wg, int quarter, int lane, const WaitGuard& g) {
+  using C = TcCfg<D>;
+  const int r = quarter * 32 + lane;  // row within the query tile = TMEM lane
+  const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+  const int ot = (C::NQT == 2) ? wg : 0;
+  // alpha of rescale step number k (counted over this accumulator) goes to slot k & 1: in
+  // single-tile mode S(j) is computed before P V j-1, so step j's alpha can be written while
+  // the correction warpgroup still reads step j-1's.
+  float* alpha_s = reinterpret_cast<float*>(gbase + C::OFF_ALPHA) + ot * 256;
+  uint32_t a_pub = 0;
+  float* stat_m = reinterpret_cast<float*>(gbase + C::OFF_STAT_M) + ot * 128;
+  float* stat_l = reinterpret_cast<float*>(gbase + C::OFF_STAT_L) + ot * 128;
+  const float sl2 = p.scale_log2;
+  const uint64_t sl2x2 = f2_pack(sl2, sl2);
+  uint32_t s_waits = 0;  // S buffers consumed by this warpgroup
+  bool ok = true;
+
+  for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x) {
+    const TcUnit w = tc_decode<D, CAUSAL>(u, p);
+    const int n = w.n[wg];
+    if (n == 0) continue;
+    const int row0 = w.row0 + wg * C::BQ;
+    const int row = row0 + r;
+    float m = -INFINITY;  // running max of scaled logits, log2 units
+    float l = 0.f;        // running sum of exp2(x - m)
+    for (int j = 0; j < n; ++j) {
+      const int buf = (C::NQT == 2) ? wg : static_cast<int>(s_waits & 1);
+      const uint32_t par = (C::NQT == 2) ? (s_waits & 1) : ((s_waits >> 1) & 1);
+      ok = warp_wait_bar(bar.s_full(buf), par, g, kStatusTimeoutSoftmax);
+      if (!ok) break;
+      ++s_waits;
+      tc_fence_after();
+      const uint32_t ts = tmem + lane_off + C::TM_S + buf * C::TM_SB;
+
+      float s[C::BK];
+      {
+        uint32_t raw_s[C::BK / 32][32];
+#pragma unroll
+        for (int c = 0; c < C::BK / 32; ++c) tmem_ld32(ts + c * 32, raw_s[c]);
+#pragma unroll
+        for (int c = 0; c < C::BK / 32; ++c) tmem_wait_ld(raw_s[c]);
+#pragma unroll
+        for (int c = 0; c < C::BK / 32; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(raw_s[c][i]);
+      }
+      const int key0 = j * C::BK;
+      const bool need_mask = (CAUSAL && key0 + C::BK - 1 > row0) || (key0 + C::BK > p.N);
+      if (need_mask) {
+#pragma unroll
+        for (int c = 0; c < C::BK; ++c) {
+          const int key = key0 + c;
+          if (key >= p.N || (CAUSAL && key > row)) s[c] = -INFINITY;
+        }
+      }
+      // Row max: 8 chains of three-input maxima over interleaved columns.
+      constexpr int KC = C::BK / 8;
+      float mx[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        float v = fmax3(s[i], s[i + 8], s[i + 16]);
+#pragma unroll
+        for (int k = 3; k + 1 < KC; k += 2) v = fmax3(v, s[i + 8 * k], s[i + 8 * (k + 1)]);
+        if ((KC - 3) % 2 == 1) v = fmaxf(v, s[i + 8 * (KC - 1)]);
+        mx[i] = v;
+      }
+      const float rmax = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7]));
+      const float m_new = fmaxf(m, rmax * sl2);
+      // alpha = exp2(m_old - m_new): 0 on the first tile, exactly 1 when the max did not grow.
+      const float alpha = (m_new == -INFINITY) ? 1.f : ex2(m - m_new);
+      if (j > 0) {
+        alpha_s[(a_pub & 1) * 128 + r] = alpha;
+        warp_arrive(bar.a_full(ot, a_pub & 1));
+        ++a_pub;
+      }
+      const float nb = (m_new == -INFINITY) ? 0.f : -m_new;
+      const uint64_t nb2 = f2_pack(nb, nb);
+      uint64_t acc[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[i] = 0ull;  // (0.f, 0.f)
+      uint32_t pk[C::BK / 2];
+#pragma unroll
+      for (int c = 0; c < C::BK; c += 2) {
+        const float2 x = f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, nb2));
+        const float p0 = ex2(x.x);
+        const float p1 = ex2(x.y);
+        pk[c >> 1] = pack_bf16x2(p0, p1);
+        acc[(c >> 1) & 3] = f2_add(acc[(c >> 1) & 3], f2_pack(p0, p1));
+      }
+      const float2 a01 = f2_unpack(f2_add(acc[0], acc[1]));
+      const float2 a23 = f2_unpack(f2_add(acc[2], acc[3]));
+      l = l * alpha + ((a01.x + a01.y) + (a23.x + a23.y));
+      m = m_new;
+#pragma unroll
+      for (int c = 0; c < C::BK / 64; ++c) {
+        uint32_t chunk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) chunk[i] = pk[c * 32 + i];
+        tmem_st32(ts + c * 32, chunk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      // P number s_waits - 1 (counted over this warpgroup) feeds P V number s_waits - 1.
+      warp_arrive(C::NQT == 2 ? bar.pv_go(ot, 0) : bar.pv_go(0, (s_waits - 1) & 1));
+    }
+    if (!ok) break;
+    stat_m[r] = m;
+    stat_l[r] = l;
+    warp_arrive(bar.l_full(ot));
+  }
+}
+
+// ------------------------------------------------------------------ correction + epilogue
+template <int D, bool CAUSAL>
+__device__ __forceinline__ void tc_correction(const TcParams& p, const TcBars<D>& bar, uint8_t* gbase, uint32_t tmem,
+                                              int quarter, int lane, const WaitGuard& g) {
+  using C = TcCfg<D>;
+  const int r = quarter * 32 + lane;
+  const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+  const float* alpha_base = reinterpret_cast<const float*>(gbase + C::OFF_ALPHA);
+  const float* stat_m = reinterpret_cast<const float*>(gbase + C::OFF_STAT_M);
+  const float* stat_l = reinterpret_cast<const float*>(gbase + C::OFF_STAT_L);
+  // o_done completes after every P V in single-tile mode (the rescale of step j
+  // must wait for P V j-1) and after the last P V of a unit in two-tile mode
+  // (S of step j being ready already implies P V j-1 finished).
+  constexpr bool PER_PV_DONE = (C::NQT == 1);
+  uint32_t a_cnt0 = 0, a_cnt1 = 0, od0 = 0, od1 = 0, lf0 = 0, lf1 = 0;
+  uint32_t go_arr = 0;  // single-tile mode: arrivals made on pv_go (= number of the P V they release)
+  bool ok = true;
+  auto release_o = [&](int t) {
+    if (C::NQT == 2) {
+      warp_arrive(bar.pv_go(t, 0));
+    } else {
+      warp_arrive(bar.pv_go(0, go_arr & 1));
+      ++go_arr;
+    }
+  };
+
+  // Rescale step j > 0 of accumulator t.
+  auto rescale = [&](int t, uint32_t& a_cnt, uint32_t& od) -> bool {
+    bool k = warp_wait_bar(bar.a_full(t, a_cnt & 1), (a_cnt >> 1) & 1, g, kStatusTimeoutSoftmax);
+    if (!k) return false;
+    const float alpha = alpha_base[t * 256 + (a_cnt & 1) * 128 + r];
+    ++a_cnt;
+    if (PER_PV_DONE) {
+      k = warp_wait_bar(bar.o_done(t), od & 1, g, kStatusTimeoutSoftmax);
+      if (!k) return false;
+      ++od;
+    }
+    if (__any_sync(0xffffffffu, alpha != 1.f)) {
+      tc_fence_after();
+      const uint32_t to = tmem + lane_off + C::TM_O + t * D;
+      const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(to + c * 32, v);
+        tmem_wait_ld(v);
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const float2 y = f2_unpack(f2_mul(f2_pack(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), a2));
+          v[i] = __float_as_uint(y.x);
+          v[i + 1] = __float_as_uint(y.y);
+        }
+        tmem_st32(to + c * 32, v);
+      }
+      tmem_wait_st();
+    }
+    tc_fence_before();
+    release_o(t);
+    return true;
+  };
+  // Epilogue of accumulator t: O / l in bf16, L = (m + log2 l) * ln 2; then O is free again.
+  auto epilogue = [&](const TcUnit& w, int t, uint32_t& od, uint32_t& lf) -> bool {
+    bool k = warp_wait_bar(bar.o_done(t), od & 1, g, kStatusTimeoutSoftmax);
+    k = k && warp_wait_bar(bar.l_full(t), lf & 1, g, kStatusTimeoutSoftmax);
+    if (!k) return false;
+    ++od;
+    ++lf;
+    tc_fence_after();
+    const float mrow = stat_m[t * 128 + r];
+    const float lrow = stat_l[t * 128 + r];
+    const float inv_l = 1.f / lrow;
+    const uint64_t il2 = f2_pack(inv_l, inv_l);
+    const int row = w.row0 + t * C::BQ + r;
+    const uint32_t to = tmem + lane_off + C::TM_O + t * D;
+    __nv_bfloat16* orow = p.o + (static_cast<size_t>(w.bh) * p.N + row) * D;
+#pragma unroll 1
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t v[32];
+      tmem_ld32(to + c * 32, v);
+      tmem_wait_ld(v);
+      uint32_t packed[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float2 y = f2_unpack(f2_mul(f2_pack(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), il2));
+        packed[i] = pack_bf16x2(y.x, y.y);
+      }
+      if (row < p.N) {
+        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+      }
+    }
+    if (row < p.N) p.lse[static_cast<size_t>(w.bh) * p.N + row] = (mrow + log2f(lrow)) * 0.69314718055994531f;
+    tc_fence_before();
+    release_o(t);  // O may be overwritten by the next unit's first P V
+    return true;
+  };
+
+  // O starts free: release it for the first unit's first P V.
+  release_o(0);
+  if (C::NO == 2) release_o(1);
+  for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x) {
+    const TcUnit w = tc_decode<D, CAUSAL>(u, p);
+    // Same order as the MMA warp's P V products: (tile 0, j), (tile 1, j), (tile 0, j+1), ...
+    for (int j = 0; ok && j < w.nmax; ++j) {
+      if (ok && j >= 1 && j < w.n[0]) ok = rescale(0, a_cnt0, od0);
+      if (C::NO == 2 && ok && j >= 1 && j < w.n[1]) ok = rescale(1, a_cnt1, od1);
+      if (ok && j == w.n[0] - 1) ok = epilogue(w, 0, od0, lf0);
+      if (C::NO == 2 && ok && j == w.n[1] - 1) ok = epilogue(w, 1, od1, lf1);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ kernel
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
     fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -148,36 +643,28 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
   uint8_t* gbase = smem_raw + (base - raw);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-
-  const uint32_t bar0 = base + C::OFF_BAR;
-  const uint32_t q_full = bar0;
-  const uint32_t q_empty = bar0 + 8;
-  auto kv_full = [&](int i) { return bar0 + 16 + 8u * i; };
-  auto kv_empty = [&](int i) { return bar0 + 16 + 8u * (C::NS + i); };
-  auto s_full = [&](int b) { return bar0 + 16 + 8u * (2 * C::NS + b); };
-  auto p_full = [&](int b) { return bar0 + 16 + 8u * (2 * C::NS + 2 + b); };
-  auto o_done = [&](int t) { return bar0 + 16 + 8u * (2 * C::NS + 4 + t); };
-  auto o_free = [&](int t) { return bar0 + 16 + 8u * (2 * C::NS + 4 + C::NO + t); };
-  const uint32_t drain = bar0 + 16 + 8u * (2 * C::NS + 4 + 2 * C::NO);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::OFF_MISC);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::OFF_MISC + 4);
+  const TcBars<D> bar{base + C::OFF_BAR};
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::OFF_TMEM_SLOT);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::OFF_ABORT);
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
-    for (int i = 0; i < C::NS; ++i) {
-      mbar_init(kv_full(i), 1);
-      mbar_init(kv_empty(i), 1);
+    mbar_init(bar.q_full(), 1);
+    mbar_init(bar.q_empty(), 1);
+    for (int i = 0; i < C::NST; ++i) {
+      mbar_init(bar.kv_full(i), 1);
+      mbar_init(bar.kv_empty(i), 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(s_full(b), 1);
-      mbar_init(p_full(b), 128);
+      // Signalled by warps (one arrival each) or by tcgen05.commit (one).
+      mbar_init(bar.s_full(b), 1);
+      mbar_init(bar.pv_go(b, 0), 8);  // 4 softmax warps + 4 correction warps
+      mbar_init(bar.pv_go(b, 1), 8);
+      mbar_init(bar.a_full(b, 0), 4);
+      mbar_init(bar.a_full(b, 1), 4);
+      mbar_init(bar.o_done(b), 1);
+      mbar_init(bar.l_full(b), 4);
     }
-    for (int t = 0; t < C::NO; ++t) {
-      mbar_init(o_done(t), 1);
-      mbar_init(o_free(t), 128);
-    }
-    mbar_init(drain, 1);
+    mbar_init(bar.drain(), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -196,326 +683,16 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitGuard g{abort_flag, p.status, p.limit_ns};
 
-  if (warp == C::LOAD_WARP) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      const uint64_t pol_q = policy_evict_first();
-      const uint64_t pol_kv = policy_evict_last();
-      uint32_t pos = 0;             // K/V loads issued so far (ring position)
-      uint32_t issued = 0;          // bit i: slot i has been loaded at least once
-      uint32_t last_par = 0;        // bit i: parity of slot i's latest load
-      int ui = 0;                   // units started by this CTA
-      int last_q = -1;              // unit index of the latest Q load
-      bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x, ++ui) {
-        const TcUnit w = tc_decode<D, CAUSAL>(u, p);
-        if (!wait_bar(q_empty, (ui & 1) ^ 1, g, kStatusTimeoutLoad)) { ok = false; break; }
-        mbar_arrive_expect_tx(q_full, C::NQT * C::Q_TILE);
-        for (int s = 0; s < C::NQT; ++s)
-          for (int r = 0; r < C::NR; ++r)
-            tma_load_3d(base + C::OFF_Q + s * C::Q_TILE + r * C::Q_REGION, &tm_q, q_full, r * C::RC,
-                        w.row0 + s * C::BQ, w.bh, pol_q);
-        last_q = ui;
-        auto load_kv = [&](const CUtensorMap* tm, int j) -> bool {
-          const int slot = pos % C::NS;
-          const uint32_t par = (pos / C::NS) & 1;
-          if (!wait_bar(kv_empty(slot), par ^ 1, g, kStatusTimeoutLoad)) return false;
-          mbar_arrive_expect_tx(kv_full(slot), C::KV_TILE);
-          for (int r = 0; r < C::NR; ++r)
-            tma_load_3d(base + C::OFF_KV + slot * C::KV_TILE + r * C::KV_REGION, tm, kv_full(slot), r * C::RC,
-                        j * C::BK, w.bh, pol_kv);
-          issued |= 1u << slot;
-          last_par = (last_par & ~(1u << slot)) | (par << slot);
-          ++pos;
-          return true;
-        };
-        for (int j = 0; ok && j < C::LA && j < w.nmax; ++j) ok = load_kv(&tm_k, j);
-        for (int j = 0; ok && j < w.nmax; ++j) {
-          ok = load_kv(&tm_v, j);
-          if (ok && j + C::LA < w.nmax) ok = load_kv(&tm_k, j + C::LA);
-        }
-      }
-      // Every issued copy must land before the CTA may exit.
-      for (int i = 0; i < C::NS; ++i)
-        if (issued & (1u << i)) wait_bar_drain(kv_full(i), (last_par >> i) & 1, g);
-      if (last_q >= 0) wait_bar_drain(q_full, last_q & 1, g);
-    }
-  } else if (warp == C::MMA_WARP) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = make_idesc_bf16(128, C::BK, 0);
-      constexpr uint32_t idesc_pv = make_idesc_bf16(128, D, 1);
-      uint32_t pos = 0;
-      uint32_t p_cnt[2] = {0, 0};   // P buffers consumed, per S buffer
-      uint32_t o_units[2] = {0, 0}; // units started, per O accumulator
-      uint32_t qk_total = 0;        // QK products issued (single-tile mode buffer alternation)
-      bool ok = true;
-      int ui = 0;
-
-      auto kv_acquire = [&](uint32_t& slot) -> bool {
-        slot = pos % C::NS;
-        const bool r = wait_bar(kv_full(slot), (pos / C::NS) & 1, g, kStatusTimeoutMma);
-        ++pos;
-        return r;
-      };
-      auto issue_qk = [&](int qt, int buf, uint32_t kslot) {
-        const uint32_t d_t = tmem + C::TM_S + buf * C::TM_SB;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const int k0 = kk * 16;
-          const uint32_t off = (k0 % C::RC) * 2;  // byte offset inside the 128-byte swizzle row
-          const uint64_t a = make_sdesc(base + C::OFF_Q + qt * C::Q_TILE + (k0 / C::RC) * C::Q_REGION + off, 16,
-                                        8 * C::SWB, C::SWZ);
-          const uint64_t b = make_sdesc(base + C::OFF_KV + kslot * C::KV_TILE + (k0 / C::RC) * C::KV_REGION + off,
-                                        16, 8 * C::SWB, C::SWZ);
-          mma_ss(d_t, a, b, idesc_qk, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(s_full(buf));
-      };
-      auto issue_pv = [&](int ot, int buf, uint32_t vslot, bool acc) {
-        const uint32_t d_t = tmem + C::TM_O + ot * D;
-        const uint32_t a_t = tmem + C::TM_S + buf * C::TM_SB;
-#pragma unroll
-        for (int kk = 0; kk < C::BK / 16; ++kk) {
-          const uint64_t b = make_sdesc(base + C::OFF_KV + vslot * C::KV_TILE + kk * 16 * C::SWB, C::KV_REGION,
-                                        8 * C::SWB, C::SWZ);
-          mma_ts(d_t, a_t + kk * 8, b, idesc_pv, (acc || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(o_done(ot));
-      };
-      // Wait for P in buffer `buf` and, on a unit's first P V into accumulator
-      // `ot`, for the epilogue of the previous unit to have read it out.
-      auto wait_p = [&](int buf, int ot, bool first) -> bool {
-        if (!wait_bar(p_full(buf), p_cnt[buf] & 1, g, kStatusTimeoutMma)) return false;
-        ++p_cnt[buf];
-        if (first) {
-          if (o_units[ot] > 0 && !wait_bar(o_free(ot), (o_units[ot] - 1) & 1, g, kStatusTimeoutMma)) return false;
-          ++o_units[ot];
-        }
-        tc_fence_after();
-        return true;
-      };
-
-      for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x, ++ui) {
-        const TcUnit w = tc_decode<D, CAUSAL>(u, p);
-        if (!wait_bar(q_full, ui & 1, g, kStatusTimeoutMma)) { ok = false; break; }
-        tc_fence_after();
-        if constexpr (C::NQT == 2) {
-          uint32_t kslot, vslot;
-          if (!(ok = kv_acquire(kslot))) break;
-          tc_fence_after();
-          for (int s = 0; s < 2; ++s)
-            if (w.n[s] > 0) issue_qk(s, s, kslot);
-          mma_commit(kv_empty(kslot));
-          if (w.nmax == 1) mma_commit(q_empty);
-          for (int j = 0; ok && j < w.nmax; ++j) {
-            if (!(ok = kv_acquire(vslot))) break;
-            bool have_k = false;
-            for (int s = 0; ok && s < 2; ++s) {
-              if (j < w.n[s]) {
-                if (!(ok = wait_p(s, s, j == 0))) break;
-                issue_pv(s, s, vslot, j > 0);
-              }
-              if (j + 1 < w.n[s]) {
-                if (!have_k) {
-                  if (!(ok = kv_acquire(kslot))) break;
-                  tc_fence_after();
-                  have_k = true;
-                }
-                issue_qk(s, s, kslot);
-              }
-            }
-            if (!ok) break;
-            mma_commit(kv_empty(vslot));
-            if (have_k) {
-              mma_commit(kv_empty(kslot));
-              if (j + 1 == w.nmax - 1) mma_commit(q_empty);
-            }
-          }
-        } else {
-          const int n = w.n[0];
-          const uint32_t qk_base = qk_total;
-          uint32_t kslot, vslot;
-          for (int t = 0; ok && t < C::LA && t < n; ++t) {
-            if (!(ok = kv_acquire(kslot))) break;
-            tc_fence_after();
-            issue_qk(0, qk_total & 1, kslot);
-            ++qk_total;
-            mma_commit(kv_empty(kslot));
-            if (t == n - 1) mma_commit(q_empty);
-          }
-          for (int j = 0; ok && j < n; ++j) {
-            if (!(ok = kv_acquire(vslot))) break;
-            const int buf = (qk_base + j) & 1;
-            if (!(ok = wait_p(buf, 0, j == 0))) break;
-            issue_pv(0, buf, vslot, j > 0);
-            mma_commit(kv_empty(vslot));
-            if (j + C::LA < n) {
-              if (!(ok = kv_acquire(kslot))) break;
-              tc_fence_after();
-              issue_qk(0, qk_total & 1, kslot);
-              ++qk_total;
-              mma_commit(kv_empty(kslot));
-              if (j + C::LA == n - 1) mma_commit(q_empty);
-            }
-          }
-        }
-      }
-      // All issued MMAs must complete before TMEM is released.
-      mma_commit(drain);
-      wait_bar_drain(drain, 0, g);
-    }
+  if (warp < C::SOFTMAX_WARPS) {
+    if constexpr (C::SPLIT_REGS) regs_increase<C::REG_SOFTMAX>();
+    tc_softmax<D, CAUSAL>(p, bar, gbase, tmem, warp >> 2, warp & 3, lane, g);
+  } else if (warp < C::SOFTMAX_WARPS + 4) {
+    if constexpr (C::SPLIT_REGS) regs_decrease<C::REG_CORR>();
+    tc_correction<D, CAUSAL>(p, bar, gbase, tmem, warp & 3, lane, g);
   } else {
-    // ------------------------------------------------------------ softmax warpgroups
-    const int wg = warp >> 2;          // query tile of the unit this warpgroup owns
-    const int quarter = warp & 3;      // TMEM lanes 32*quarter .. +31
-    const int r = quarter * 32 + lane; // row within the query tile
-    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const float sl2 = p.scale_log2;
-    constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only if the max grew > 2^8
-    uint32_t s_waits = 0;   // S buffers consumed by this warpgroup
-    uint32_t pv_done = 0;   // P V products into this warpgroup's O completed in earlier units
-    bool ok = true;
-    const int ot = (C::NQT == 2) ? wg : 0;
-
-    for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x) {
-      const TcUnit w = tc_decode<D, CAUSAL>(u, p);
-      const int n = w.n[wg];
-      if (n == 0) continue;
-      const int row0 = w.row0 + wg * C::BQ;
-      const int row = row0 + r;
-      float m = -INFINITY;  // running max of scaled logits, log2 units
-      float l = 0.f;        // running sum of exp2(x - m)
-      float lw = 0.f;       // the same sum over the bf16-rounded weights
-      for (int j = 0; j < n; ++j) {
-        const int buf = (C::NQT == 2) ? wg : static_cast<int>(s_waits & 1);
-        const uint32_t par = (C::NQT == 2) ? (s_waits & 1) : ((s_waits >> 1) & 1);
-        ok = wait_bar(s_full(buf), par, g, kStatusTimeoutSoftmax);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        ++s_waits;
-        tc_fence_after();
-        const uint32_t ts = tmem + lane_off + C::TM_S + buf * C::TM_SB;
-
-        float s[C::BK];
-        {
-          uint32_t raw_s[C::BK / 32][32];
-#pragma unroll
-          for (int c = 0; c < C::BK / 32; ++c) tmem_ld32(ts + c * 32, raw_s[c]);
-#pragma unroll
-          for (int c = 0; c < C::BK / 32; ++c) tmem_wait_ld(raw_s[c]);
-#pragma unroll
-          for (int c = 0; c < C::BK / 32; ++c)
-#pragma unroll
-            for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(raw_s[c][i]);
-        }
-        const int key0 = j * C::BK;
-        const bool need_mask = (CAUSAL && key0 + C::BK - 1 > row0) || (key0 + C::BK > p.N);
-        if (need_mask) {
-#pragma unroll
-          for (int c = 0; c < C::BK; ++c) {
-            const int key = key0 + c;
-            if (key >= p.N || (CAUSAL && key > row)) s[c] = -INFINITY;
-          }
-        }
-        float mx[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mx[i] = s[i];
-#pragma unroll
-        for (int c = 8; c < C::BK; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
-        const float rmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-        const float m_cand = fmaxf(m, rmax * sl2);
-        const bool grow = m_cand > m + kRescaleThreshold;  // always true on the first tile
-        const float m_new = grow ? m_cand : m;
-        const float alpha = grow ? ex2(m - m_new) : 1.f;   // ex2(-inf) = 0 on the first tile
-        const float nbase = (m_new == -INFINITY) ? 0.f : -m_new;
-        // Two row sums: lsum of the fp32 weights (for L, the logsumexp) and
-        // wsum of the bf16-rounded weights that P V multiplies (for O / l, so
-        // the division normalises exactly the weights that were applied).
-        float lsum[4], wsum[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) lsum[i] = wsum[i] = 0.f;
-        uint32_t pk[C::BK / 2];
-#pragma unroll
-        for (int c = 0; c < C::BK; c += 2) {
-          const float p0 = ex2(fmaf(s[c], sl2, nbase));
-          const float p1 = ex2(fmaf(s[c + 1], sl2, nbase));
-          const uint32_t w = pack_bf16x2(p0, p1);
-          pk[c >> 1] = w;
-          lsum[(c >> 1) & 3] += p0 + p1;
-          wsum[(c >> 1) & 3] += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
-        }
-        l = l * alpha + ((lsum[0] + lsum[1]) + (lsum[2] + lsum[3]));
-        lw = lw * alpha + ((wsum[0] + wsum[1]) + (wsum[2] + wsum[3]));
-        m = m_new;
-#pragma unroll
-        for (int c = 0; c < C::BK / 64; ++c) {
-          uint32_t chunk[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) chunk[i] = pk[c * 32 + i];
-          tmem_st32(ts + c * 32, chunk);
-        }
-        tmem_wait_st();
-        if (j > 0) {
-          // Observe the completion of P V number j-1 on this accumulator.  Every
-          // completion of o_done is waited for in order: a parity wait that ran
-          // two phases ahead of the barrier would read an older phase as done.
-          // (At most P V j-1 can be outstanding: P V j needs this tile's P.)
-          ok = wait_bar(o_done(ot), (pv_done + j - 1) & 1, g, kStatusTimeoutSoftmax);
-          ok = __all_sync(0xffffffffu, ok);
-          if (!ok) break;
-        }
-        // Rescale the O accumulator of this row when its max grew past the threshold.
-        const bool need = grow && j > 0;
-        if (__any_sync(0xffffffffu, need)) {
-          tc_fence_after();
-          const uint32_t to = tmem + lane_off + C::TM_O + ot * D;
-#pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t v[32];
-            tmem_ld32(to + c * 32, v);
-            tmem_wait_ld(v);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-            tmem_st32(to + c * 32, v);
-          }
-          tmem_wait_st();
-        }
-        tc_fence_before();
-        mbar_arrive(p_full(buf));
-      }
-      if (!ok) break;
-      // ---- epilogue: O / l in bf16, L = (m + log2 l) * ln 2
-      // P V number n-1 is the only one not yet observed (see above).
-      ok = wait_bar(o_done(ot), (pv_done + n - 1) & 1, g, kStatusTimeoutSoftmax);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      pv_done += n;
-      tc_fence_after();
-      const float inv_l = 1.f / lw;
-      const uint32_t to = tmem + lane_off + C::TM_O + ot * D;
-      __nv_bfloat16* orow = p.o + (static_cast<size_t>(w.bh) * p.N + row) * D;
-#pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(to + c * 32, v);
-        tmem_wait_ld(v);
-        uint32_t packed[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          packed[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * inv_l, __uint_as_float(v[2 * i + 1]) * inv_l);
-        if (row < p.N) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
-        }
-      }
-      if (row < p.N) p.lse[static_cast<size_t>(w.bh) * p.N + row] = (m + log2f(l)) * 0.69314718055994531f;
-      tc_fence_before();
-      mbar_arrive(o_free(ot));
-    }
+    if constexpr (C::SPLIT_REGS) regs_decrease<C::REG_OTHER>();
+    if (warp == C::LOAD_WARP && lane == 0) tc_producer<D, CAUSAL>(&tm_q, &tm_k, &tm_v, p, bar, base, g);
+    if (warp == C::MMA_WARP && lane == 0) tc_mma<D, CAUSAL>(p, bar, base, tmem, g);
   }
 
   __syncwarp();

@@ -14,6 +14,20 @@ int launch_tc_impl(const void* q, const void* k, const void* v, void* o, float* 
                    const LaunchCtx& ctx) {
   using C = TcCfg<D>;
   auto kernel = fa_fwd_tc_kernel<D, CAUSAL>;
+  if constexpr (C::SPLIT_REGS) {
+    // The warpgroups re-split the registers the block was launched with
+    // (setmaxnreg); the split is sized for exactly LAUNCH_REGS per thread.  A
+    // build with any other count would make setmaxnreg.inc wait forever, so it
+    // is refused here.
+    static int checked_regs = -1;
+    if (checked_regs < 0) {
+      cudaFuncAttributes attr;
+      cudaError_t ea = cudaFuncGetAttributes(&attr, kernel);
+      if (ea != cudaSuccess) return static_cast<int>(ea);
+      checked_regs = attr.numRegs;
+    }
+    if (checked_regs != C::LAUNCH_REGS) return -2;
+  }
   // The attribute is per function and device; setting it again is cheap and idempotent.
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
   if (e != cudaSuccess) return static_cast<int>(e);

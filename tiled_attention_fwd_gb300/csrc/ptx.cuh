@@ -50,6 +50,19 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity)
   return ok;
 }
 
+// Non-blocking test of the phase with parity `parity`.
+__device__ __forceinline__ uint32_t mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred P1;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 P1, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, P1;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok;
+}
+
 // Error bits written to the device status word.
 enum : int {
   kStatusTimeoutLoad = 1 << 0,
@@ -81,6 +94,31 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Wa
       return false;
     }
   }
+}
+
+// Warp-level forms.  Every lane waits (a warp whose lanes all wait on the
+// barrier is suspended and resumed together), the outcome is made uniform
+// across the warp; arrivals are made by lane 0 for the whole warp after
+// __syncwarp, which orders the memory operations of the warp's lanes before
+// lane 0's release.  A barrier signalled this way counts one arrival per warp.
+__device__ __forceinline__ bool warp_wait_bar(uint32_t bar, uint32_t parity, const WaitGuard& g, int code) {
+  const bool ok = wait_bar(bar, parity, g, code);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Lane 0 waits for the warp (a non-blocking test first, then the bounded
+// wait); the outcome is broadcast and __syncwarp orders the other lanes after
+// lane 0's acquire.  For warps whose lanes do nothing but issue on lane 0.
+__device__ __forceinline__ bool leader_wait_bar(uint32_t bar, uint32_t parity, const WaitGuard& g, int code) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = (mbar_test_wait(bar, parity) || wait_bar(bar, parity, g, code)) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  return ok != 0;
+}
+
+__device__ __forceinline__ void warp_arrive(uint32_t bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
 // ------------------------------------------------------------------ TMA
@@ -228,12 +266,57 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// ------------------------------------------------------------------ register budget
+// Re-split the block's registers between warpgroups (all four warps of a
+// warpgroup execute the same instruction).
+template <uint32_t N>
+__device__ __forceinline__ void regs_increase() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_decrease() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ------------------------------------------------------------------ math
 // Hardware base-2 exponential (MUFU), flushes denormals; ex2(-inf) = +0.
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Paired fp32 arithmetic (one instruction on two lanes of a 64-bit register pair).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 f2_unpack(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 // Two fp32 values to one bf16x2 word, round to nearest even; `lo` in bits 0..15.
