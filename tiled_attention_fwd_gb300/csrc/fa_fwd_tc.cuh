@@ -152,6 +152,15 @@ __device__ __forceinline__ TcUnit tc_decode(int u, const TcParams& p) {
   return w;
 }
 
+// k-th work unit of this CTA.  Units are numbered heaviest first; CTAs take
+// them in rounds of gridDim.x, alternating direction every round (a snake),
+// so the CTA that takes the heaviest unit of one round takes the lightest of
+// the next and causal work evens out without any shared counter.
+__device__ __forceinline__ int tc_unit(int k) {
+  const int g = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
+  return k * g + ((k & 1) ? g - 1 - b : b);
+}
+
 // Wait without looking at the abort flag (used to drain in-flight copies and
 // MMAs before the CTA exits); still time-limited.
 __device__ __forceinline__ bool wait_bar_drain(uint32_t bar, uint32_t parity, const WaitGuard& g) {
@@ -212,7 +221,7 @@ __device__ __forceinline__ void tc_producer(const CUtensorMap* tm_q, const CUten
   auto load_tile = [&](const CUtensorMap* tm, uint32_t dst, uint32_t full, int j, int bh) {
     for (int r = 0; r < C::NR; ++r) tma_load_3d(dst + r * C::KV_REGION, tm, full, r * C::RC, j * C::BK, bh, pol_kv);
   };
-  for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x, ++ui) {
+  for (int uk = 0, u; ok && (u = tc_unit(uk)) < p.total_units; ++uk, ++ui) {
     const TcUnit w = tc_decode<D, CAUSAL>(u, p);
     if (!wait_bar(bar.q_empty(), (ui & 1) ^ 1, g, kStatusTimeoutLoad)) {
       ok = false;
@@ -336,7 +345,7 @@ __device__ __forceinline__ void tc_mma(const TcParams& p, const TcBars<D>& bar, 
     return true;
   };
 
-  for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x, ++ui) {
+  for (int uk = 0, u; ok && (u = tc_unit(uk)) < p.total_units; ++uk, ++ui) {
     const TcUnit w = tc_decode<D, CAUSAL>(u, p);
     if (!wait(bar.q_full(), ui & 1)) {
       ok = false;
@@ -422,7 +431,7 @@ __device__ __forceinline__ void tc_softmax(const TcParams& p, const TcBars<D>& b
   uint32_t s_waits = 0;  // S buffers consumed by this warpgroup
   bool ok = true;
 
-  for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x) {
+  for (int uk = 0, u; ok && (u = tc_unit(uk)) < p.total_units; ++uk) {
     const TcUnit w = tc_decode<D, CAUSAL>(u, p);
     const int n = w.n[wg];
     if (n == 0) continue;
@@ -619,7 +628,7 @@ __device__ __forceinline__ void tc_correction(const TcParams& p, const TcBars<D>
   // O starts free: release it for the first unit's first P V.
   release_o(0);
   if (C::NO == 2) release_o(1);
-  for (int u = blockIdx.x; ok && u < p.total_units; u += gridDim.x) {
+  for (int uk = 0, u; ok && (u = tc_unit(uk)) < p.total_units; ++uk) {
     const TcUnit w = tc_decode<D, CAUSAL>(u, p);
     // Same order as the MMA warp's P V products: (tile 0, j), (tile 1, j), (tile 0, j+1), ...
     for (int j = 0; ok && j < w.nmax; ++j) {
