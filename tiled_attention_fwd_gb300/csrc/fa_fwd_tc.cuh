@@ -19,21 +19,22 @@
 //     while the softmax computes P, and runs the epilogue (O / l in bf16,
 //     L = m + log l) so the softmax can start the next work unit at once;
 //   * one MMA warp: tcgen05.mma S = Q K^T into TMEM, then O += P V with P read
-//     from TMEM and V from shared memory;
+//     from TMEM and V from shared memory, issued by an elected lane;
 //   * one TMA producer warp: Q tiles and a ring of K/V stages in 128-byte
 //     swizzled shared memory, each stage guarded by full/empty mbarriers.
 // For d <= 128 a work unit is two query tiles (256 rows) that share every K/V
 // tile, and the MMA warp alternates between them so one tile's softmax
 // overlaps the other tile's matrix products; for d = 256 a work unit is one
 // query tile with a double-buffered S.  Work units (batch*head, query block)
-// are ordered heaviest first for the causal mask and strided over the
-// persistent CTAs; key tiles wholly in the future of a query tile are never
-// loaded or multiplied.
+// are ordered heaviest first for the causal mask and dealt to the persistent
+// CTAs in snake order; key tiles wholly in the future of a query tile are
+// never loaded or multiplied.
 //
-// The tensor core executes MMAs about as fast as one thread can issue them,
-// so the MMA warp is kept lean: one readiness barrier per P V product (the
-// softmax's P and the correction's O meet there), one barrier per K/V stage,
-// descriptors built once.
+// The tensor core executes MMAs about as fast as the MMA warp can issue them
+// while it shares its scheduler with softmax and correction warps, so the
+// issuer is kept lean: one readiness barrier per P V product (the softmax's
+// P and the correction's O meet there), one barrier per K/V stage,
+// descriptors built once and stepped with 32-bit adds.
 //
 // Every mbarrier phase is waited for in order by its consumer: a parity wait
 // issued two phases ahead of a barrier would read an older phase as complete.
@@ -263,17 +264,29 @@ __device__ __forceinline__ void tc_producer(const CUtensorMap* tm_q, const CUten
 }
 
 // ------------------------------------------------------------------ MMA issuer
-// Run by one thread (lane 0 of the MMA warp): under load from the softmax
-// warps sharing its scheduler, a lone thread issues tcgen05.mma at the tensor
-// core's rate, while a warp that re-converges around each group of MMAs does
-// not.  Descriptors are built once: a tile position or K step only adds a
-// constant to the address field (bits 0..13 hold address / 16, and no shared
-// address reaches 2^18).
+// One warp issues every tcgen05.mma and tcgen05.commit of the CTA: all its
+// lanes run the loop (so descriptors and addresses are warp-uniform values)
+// and elect.sync picks the lane that issues each operation.  Under load from
+// the softmax and correction warps sharing its scheduler this sustains the
+// tensor core's rate better than a lone lane-0 thread.  The order lets one
+// tile's softmax overlap the other tile's products:
+// P V_0 j, S_0 j+1, P V_1 j, S_1 j+1.  Products issued by one warp complete
+// in issue order: P V j finishes before S of key tile j + 1 overwrites the
+// S/P buffer, and S of key tile j being ready implies P V j - 1 finished.
+// (Two issuers, one per tile, would interleave the tiles' products on the
+// tensor core and lengthen each tile's softmax-to-softmax cycle.)
+//
+// Descriptors are kept as (low, high) words and built once: a tile position
+// or K step only adds a constant to the low word's address field (bits 0..13
+// hold address / 16, and no shared address reaches 2^18, so it never carries).
 template <int D>
 struct TcMma {
   using C = TcCfg<D>;
   static constexpr uint32_t IDESC_QK = make_idesc_bf16(128, C::BK, 0);
   static constexpr uint32_t IDESC_PV = make_idesc_bf16(128, D, 1);
+  // K-major (Q, K) and MN-major (V) operands share the stride byte offset
+  // (8 rows of the swizzle span) and the swizzle mode.
+  static constexpr uint32_t DESC_HI = sdesc_hi(8 * C::SWB, C::SWZ);
   // Address-field increments (16-byte units).
   static constexpr __host__ __device__ uint32_t q_step(int kk) {
     return ((kk * 16 / C::RC) * C::Q_REGION + (kk * 16 % C::RC) * 2) >> 4;
@@ -286,33 +299,35 @@ struct TcMma {
   static constexpr uint32_t QTILE_STEP = C::Q_TILE >> 4;
 
   uint32_t tmem;
-  uint64_t dq0;   // Q tile 0, K-major
-  uint64_t dk0;   // K/V tile position 0, K-major (K as the B operand of S = Q K^T)
-  uint64_t dv0;   // K/V tile position 0, MN-major (V as the B operand of O = P V)
+  uint32_t q_lo;  // Q tile 0, K-major
+  uint32_t k_lo;  // K/V tile position 0, K-major (K as the B operand of S = Q K^T)
+  uint32_t v_lo;  // K/V tile position 0, MN-major (V as the B operand of O = P V)
 
   __device__ __forceinline__ TcMma(uint32_t tmem_, uint32_t base) : tmem(tmem_) {
-    dq0 = make_sdesc(base + C::OFF_Q, 16, 8 * C::SWB, C::SWZ);
-    dk0 = make_sdesc(base + C::OFF_KV, 16, 8 * C::SWB, C::SWZ);
-    dv0 = make_sdesc(base + C::OFF_KV, C::KV_REGION, 8 * C::SWB, C::SWZ);
+    q_lo = sdesc_lo(base + C::OFF_Q, 16);
+    k_lo = sdesc_lo(base + C::OFF_KV, 16);
+    v_lo = sdesc_lo(base + C::OFF_KV, C::KV_REGION);
   }
   // S[buf] = Q[qt] K^T with K at tile position kpos; completion on s_full_bar.
   __device__ __forceinline__ void qk(int qt, int buf, uint32_t kpos, uint32_t s_full_bar) const {
     const uint32_t d_t = tmem + C::TM_S + buf * C::TM_SB;
-    const uint64_t a = dq0 + qt * QTILE_STEP;
-    const uint64_t b = dk0 + kpos * TILE_STEP;
+    const uint32_t a = q_lo + qt * QTILE_STEP;
+    const uint32_t b = k_lo + kpos * TILE_STEP;
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) mma_ss(d_t, a + q_step(kk), b + k_step(kk), IDESC_QK, kk > 0 ? 1u : 0u);
-    mma_commit(s_full_bar);
+    for (int kk = 0; kk < D / 16; ++kk)
+      mma_ss_elect(d_t, a + q_step(kk), DESC_HI, b + k_step(kk), DESC_HI, IDESC_QK, kk > 0 ? 1u : 0u);
+    commit(s_full_bar);
   }
   // O[ot] (+)= P[buf] V with V at tile position vpos.
   __device__ __forceinline__ void pv(int ot, int buf, uint32_t vpos, bool acc) const {
     const uint32_t d_t = tmem + C::TM_O + ot * D;
     const uint32_t a_t = tmem + C::TM_S + buf * C::TM_SB;
-    const uint64_t b = dv0 + vpos * TILE_STEP;
+    const uint32_t b = v_lo + vpos * TILE_STEP;
 #pragma unroll
-    for (int kk = 0; kk < C::BK / 16; ++kk) mma_ts(d_t, a_t + kk * 8, b + v_step(kk), IDESC_PV, (acc || kk > 0) ? 1u : 0u);
+    for (int kk = 0; kk < C::BK / 16; ++kk)
+      mma_ts_elect(d_t, a_t + kk * 8, b + v_step(kk), DESC_HI, IDESC_PV, (acc || kk > 0) ? 1u : 0u);
   }
-  __device__ __forceinline__ void commit(uint32_t bar) const { mma_commit(bar); }
+  __device__ __forceinline__ void commit(uint32_t bar) const { mma_commit_elect(bar); }
 };
 
 template <int D, bool CAUSAL>
@@ -320,9 +335,11 @@ __device__ __forceinline__ void tc_mma(const TcParams& p, const TcBars<D>& bar, 
                                        const WaitGuard& g) {
   using C = TcCfg<D>;
   const TcMma<D> M(tmem, base);
-  // Single-thread wait: a non-blocking test first, then the bounded wait.
+  // Every lane waits (a non-blocking test first, then the bounded wait); the
+  // outcome is made warp-uniform.
   auto wait = [&](uint32_t b, uint32_t par) -> bool {
-    return mbar_test_wait(b, par) || wait_bar(b, par, g, kStatusTimeoutMma);
+    const bool r = mbar_test_wait(b, par) || wait_bar(b, par, g, kStatusTimeoutMma);
+    return __all_sync(0xffffffffu, r);
   };
   uint32_t pos = 0;               // K/V stages consumed
   uint32_t go0 = 0, go1 = 0;      // pv_go phases consumed, per O accumulator
@@ -409,6 +426,7 @@ __device__ __forceinline__ void tc_mma(const TcParams& p, const TcBars<D>& bar, 
   // All issued MMAs must complete before TMEM is released.
   M.commit(bar.drain());
   wait_bar_drain(bar.drain(), 0, g);
+  __syncwarp();
 }
 
 // ------------------------------------------------------------------ softmax
@@ -494,26 +512,25 @@ __device__ __forceinline__ void tc_softmax(const TcParams& p, const TcBars<D>& b
       uint64_t acc[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[i] = 0ull;  // (0.f, 0.f)
-      uint32_t pk[C::BK / 2];
+      // P in chunks of 64 columns (32 bf16x2 words), each stored to TMEM as soon
+      // as it is packed.
 #pragma unroll
-      for (int c = 0; c < C::BK; c += 2) {
-        const float2 x = f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, nb2));
-        const float p0 = ex2(x.x);
-        const float p1 = ex2(x.y);
-        pk[c >> 1] = pack_bf16x2(p0, p1);
-        acc[(c >> 1) & 3] = f2_add(acc[(c >> 1) & 3], f2_pack(p0, p1));
+      for (int h = 0; h < C::BK / 64; ++h) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 64 * h; c < 64 * h + 64; c += 2) {
+          const float2 x = f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, nb2));
+          const float p0 = ex2(x.x);
+          const float p1 = ex2(x.y);
+          pk[(c >> 1) & 31] = pack_bf16x2(p0, p1);
+          acc[(c >> 1) & 3] = f2_add(acc[(c >> 1) & 3], f2_pack(p0, p1));
+        }
+        tmem_st32(ts + h * 32, pk);
       }
       const float2 a01 = f2_unpack(f2_add(acc[0], acc[1]));
       const float2 a23 = f2_unpack(f2_add(acc[2], acc[3]));
       l = l * alpha + ((a01.x + a01.y) + (a23.x + a23.y));
       m = m_new;
-#pragma unroll
-      for (int c = 0; c < C::BK / 64; ++c) {
-        uint32_t chunk[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) chunk[i] = pk[c * 32 + i];
-        tmem_st32(ts + c * 32, chunk);
-      }
       tmem_wait_st();
       tc_fence_before();
       // P number s_waits - 1 (counted over this warpgroup) feeds P V number s_waits - 1.
@@ -701,7 +718,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
   } else {
     if constexpr (C::SPLIT_REGS) regs_decrease<C::REG_OTHER>();
     if (warp == C::LOAD_WARP && lane == 0) tc_producer<D, CAUSAL>(&tm_q, &tm_k, &tm_v, p, bar, base, g);
-    if (warp == C::MMA_WARP && lane == 0) tc_mma<D, CAUSAL>(p, bar, base, tmem, g);
+    if (warp == C::MMA_WARP) tc_mma<D, CAUSAL>(p, bar, base, tmem, g);
   }
 
   __syncwarp();

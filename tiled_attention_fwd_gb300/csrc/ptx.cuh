@@ -171,34 +171,6 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (bf16 inputs, fp32 accumulator).
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred P1;\n\t"
-      "setp.ne.b32 P1, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, P1;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem], kind::f16; A is read from tensor memory.
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred P1;\n\t"
-      "setp.ne.b32 P1, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, P1;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Arrive once on `bar` when every tcgen05.mma issued so far by this thread has completed.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-               : "memory");
-}
-
 // Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator, bf16 A and B,
 // A K-major, B K-major (b_mn_major = 0) or MN-major (1), shape M x N.
 __host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, int b_mn_major) {
@@ -211,16 +183,54 @@ __host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, int b_mn_ma
          | (static_cast<uint32_t>(M >> 4) << 24);     // M / 16
 }
 
-// Shared-memory matrix descriptor (tcgen05 format).  `swizzle`: 2 = 128-byte,
-// 4 = 64-byte, 6 = 32-byte, 0 = none.  lbo/sbo are byte offsets.
-__device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t swizzle) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
-  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
-  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
-  d |= static_cast<uint64_t>(1u) << 46;  // fixed constant 0b001 in bits 46..48
-  d |= static_cast<uint64_t>(swizzle & 7u) << 61;
-  return d;
+// Shared-memory matrix descriptor (tcgen05 format), as two 32-bit words.
+// Low word: start address / 16 in bits 0..13, leading byte offset / 16 in
+// bits 16..29.  High word: stride byte offset / 16 in bits 0..13 (bits
+// 32..45), the fixed 0b001 at bit 14 (bit 46), swizzle mode in bits 29..31
+// (bits 61..63; 2 = 128-byte, 4 = 64-byte).
+__host__ __device__ constexpr uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo) {
+  return ((saddr >> 4) & 0x3FFFu) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+__host__ __device__ constexpr uint32_t sdesc_hi(uint32_t sbo, uint32_t swizzle) {
+  return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | ((swizzle & 7u) << 29);
+}
+
+// tcgen05.mma kind::f16 with the descriptors passed as (low, high) words, so
+// that stepping through a tile is a 32-bit add on the low word.  Warp-wide:
+// every lane of the warp executes them and one elected lane issues (the
+// operands are warp-uniform).  _ss: A and B in shared memory; _ts: A in
+// tensor memory.
+__device__ __forceinline__ void mma_ss_elect(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
+                                               uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred P1, PE;\n\t.reg .b64 DA, DB;\n\t"
+      "setp.ne.b32 P1, %6, 0;\n\t"
+      "mov.b64 DA, {%1, %2};\n\t"
+      "mov.b64 DB, {%3, %4};\n\t"
+      "elect.sync _|PE, 0xffffffff;\n\t"
+      "@PE tcgen05.mma.cta_group::1.kind::f16 [%0], DA, DB, %5, P1;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred P1, PE;\n\t.reg .b64 DB;\n\t"
+      "setp.ne.b32 P1, %5, 0;\n\t"
+      "mov.b64 DB, {%2, %3};\n\t"
+      "elect.sync _|PE, 0xffffffff;\n\t"
+      "@PE tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], DB, %4, P1;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive once on `bar` when every tcgen05 operation the warp issued so far
+// has completed (issued by one elected lane).
+__device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred PE;\n\t"
+      "elect.sync _|PE, 0xffffffff;\n\t"
+      "@PE tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+      : "memory");
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: this thread's TMEM lane, columns [col, col+32).
