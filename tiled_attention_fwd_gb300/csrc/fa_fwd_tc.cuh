@@ -75,7 +75,7 @@ struct TcCfg {
   static constexpr int KV_TILE = BK * D * 2;
   static constexpr int NO = NQT;                       // O accumulators in TMEM
   // Shared memory: [Q tiles][K/V stages][misc]; misc = barriers, alpha, m/l, TMEM address, abort flag.
-  static constexpr int MISC = 6144;
+  static constexpr int MISC = 7168;
   static constexpr int SMEM_LIMIT = 227 * 1024;
   // A K/V stage holds two tiles: V_j and K_{j+LA} (the first stage of a unit: K_0 .. K_{LA-1}).
   static constexpr int STAGE = 2 * KV_TILE;
@@ -86,9 +86,12 @@ struct TcCfg {
   static constexpr int OFF_MISC = OFF_KV + NST * STAGE;
   static constexpr int OFF_BAR = OFF_MISC;                    // 64 barriers at most
   static constexpr int OFF_ALPHA = OFF_MISC + 512;            // float [NO][2][128] (by step parity)
-  static constexpr int OFF_STAT_M = OFF_ALPHA + 4 * 128 * 4;  // float [NO][128]
-  static constexpr int OFF_STAT_L = OFF_STAT_M + 2 * 128 * 4; // float [NO][128]
-  static constexpr int OFF_TMEM_SLOT = OFF_STAT_L + 2 * 128 * 4;
+  // m and l of a finished unit, double-buffered by the parity of the unit's
+  // index within the CTA: the softmax may finish the next unit (one key tile)
+  // while the correction warpgroup still reads this one's.
+  static constexpr int OFF_STAT_M = OFF_ALPHA + 4 * 128 * 4;  // float [2][NO][128]
+  static constexpr int OFF_STAT_L = OFF_STAT_M + 4 * 128 * 4; // float [2][NO][128]
+  static constexpr int OFF_TMEM_SLOT = OFF_STAT_L + 4 * 128 * 4;
   static constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
   static constexpr int SMEM_USED = OFF_MISC + MISC + 1024;    // + slack for 1024-byte alignment
   // At least ~120 KB so that a second CTA never shares the SM (and its TMEM).
@@ -180,32 +183,41 @@ template <int D>
 struct TcBars {
   using C = TcCfg<D>;
   uint32_t b0;
-  __device__ __forceinline__ uint32_t q_full() const { return b0; }
-  __device__ __forceinline__ uint32_t q_empty() const { return b0 + 8; }
-  __device__ __forceinline__ uint32_t kv_full(int i) const { return b0 + 16 + 8u * i; }
-  __device__ __forceinline__ uint32_t kv_empty(int i) const { return b0 + 16 + 8u * (C::NST + i); }
-  __device__ __forceinline__ uint32_t s_full(int b) const { return b0 + 16 + 8u * (2 * C::NST + b); }
+  // Q tile t loaded / free again (one phase per work unit).
+  __device__ __forceinline__ uint32_t q_full(int t) const { return b0 + 8u * t; }
+  __device__ __forceinline__ uint32_t q_empty(int t) const { return b0 + 16 + 8u * t; }
+  __device__ __forceinline__ uint32_t kv_full(int i) const { return b0 + 32 + 8u * i; }
+  __device__ __forceinline__ uint32_t kv_empty(int i) const { return b0 + 32 + 8u * (C::NST + i); }
+  __device__ __forceinline__ uint32_t s_full(int b) const { return b0 + 32 + 8u * (2 * C::NST + b); }
   // P V number g into accumulator t may start: P written (4 softmax warps) and
   // O ready (4 correction warps: rescaled, or released by the previous
   // epilogue).  Two-tile mode: barrier (t, 0).  Single-tile mode: barrier
   // (0, g & 1), each completing once per two P V products, because there S of
   // step j+1 is computed before P V j and the softmax may post P j+1 while
   // P V j still waits for the correction warpgroup.
-  __device__ __forceinline__ uint32_t pv_go(int t, int k) const { return b0 + 16 + 8u * (2 * C::NST + 2 + 2 * t + k); }
+  __device__ __forceinline__ uint32_t pv_go(int t, int k) const { return b0 + 32 + 8u * (2 * C::NST + 2 + 2 * t + k); }
   // alpha of rescale step k of accumulator t published: barrier (t, k & 1), each
   // completing once per two steps (single-tile mode lets the softmax run two
   // steps ahead of the correction warpgroup).
-  __device__ __forceinline__ uint32_t a_full(int t, int k) const { return b0 + 16 + 8u * (2 * C::NST + 6 + 2 * t + k); }
-  __device__ __forceinline__ uint32_t o_done(int t) const { return b0 + 16 + 8u * (2 * C::NST + 10 + t); }
-  __device__ __forceinline__ uint32_t l_full(int t) const { return b0 + 16 + 8u * (2 * C::NST + 12 + t); }
-  __device__ __forceinline__ uint32_t drain() const { return b0 + 16 + 8u * (2 * C::NST + 14); }
-  static constexpr int COUNT = 2 + 2 * C::NST + 15;
+  __device__ __forceinline__ uint32_t a_full(int t, int k) const { return b0 + 32 + 8u * (2 * C::NST + 6 + 2 * t + k); }
+  __device__ __forceinline__ uint32_t o_done(int t) const { return b0 + 32 + 8u * (2 * C::NST + 10 + t); }
+  __device__ __forceinline__ uint32_t l_full(int t) const { return b0 + 32 + 8u * (2 * C::NST + 12 + t); }
+  __device__ __forceinline__ uint32_t drain() const { return b0 + 32 + 8u * (2 * C::NST + 14); }
+  static constexpr int COUNT = 4 + 2 * C::NST + 15;
   static_assert(COUNT * 8 <= 512, "barrier area");
 };
 
 // ------------------------------------------------------------------ TMA producer
 // Run by one thread (lane 0 of the producer warp).
-// Stage sequence of a unit: {K_0 .. K_{LA-1}}, then {V_j, K_{j+LA}} for j < nmax.
+//
+// Two-tile mode: the CTA's units form one continuous stream, so that the
+// next unit's first S products can be issued while the current unit's last
+// P V products run.  Stages: {K_0} of the first unit, then {V_j, K_{j+1}} for
+// j < nmax of each unit, where the K slot of a unit's last stage holds K_0 of
+// the next unit.  Q tile t of the next unit is loaded after that last stage,
+// as soon as the current unit's last S_t product has completed (q_empty(t)).
+//
+// Single-tile mode: per unit, Q, then {K_0, K_1}, then {V_j, K_{j+2}}.
 template <int D, bool CAUSAL>
 __device__ __forceinline__ void tc_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                             const TcParams& p, const TcBars<D>& bar, uint32_t base,
@@ -216,51 +228,89 @@ __device__ __forceinline__ void tc_producer(const CUtensorMap* tm_q, const CUten
   uint32_t pos = 0;       // stages issued so far
   uint32_t issued = 0;    // bit i: stage i has been loaded at least once
   uint32_t last_par = 0;  // bit i: parity of stage i's latest load
-  int ui = 0;             // units started by this CTA
-  int last_q = -1;        // unit index of the latest Q load
+  int last_q[2] = {-1, -1};  // per Q tile: index (within this CTA) of the latest unit whose tile was loaded
   bool ok = true;
   auto load_tile = [&](const CUtensorMap* tm, uint32_t dst, uint32_t full, int j, int bh) {
     for (int r = 0; r < C::NR; ++r) tma_load_3d(dst + r * C::KV_REGION, tm, full, r * C::RC, j * C::BK, bh, pol_kv);
   };
-  for (int uk = 0, u; ok && (u = tc_unit(uk)) < p.total_units; ++uk, ++ui) {
-    const TcUnit w = tc_decode<D, CAUSAL>(u, p);
-    if (!wait_bar(bar.q_empty(), (ui & 1) ^ 1, g, kStatusTimeoutLoad)) {
-      ok = false;
-      break;
-    }
-    mbar_arrive_expect_tx(bar.q_full(), C::NQT * C::Q_TILE);
-    for (int s = 0; s < C::NQT; ++s)
+  // Q tiles of unit x, the qi-th unit of this CTA.
+  auto load_q = [&](const TcUnit& x, int qi) -> bool {
+    for (int t = 0; t < C::NQT; ++t) {
+      if (!wait_bar(bar.q_empty(t), (qi & 1) ^ 1, g, kStatusTimeoutLoad)) return false;
+      mbar_arrive_expect_tx(bar.q_full(t), C::Q_TILE);
       for (int r = 0; r < C::NR; ++r)
-        tma_load_3d(base + C::OFF_Q + s * C::Q_TILE + r * C::Q_REGION, tm_q, bar.q_full(), r * C::RC,
-                    w.row0 + s * C::BQ, w.bh, pol_q);
-    last_q = ui;
-    for (int t = -1; ok && t < w.nmax; ++t) {
-      const int st = pos % C::NST;
-      const uint32_t par = (pos / C::NST) & 1;
-      if (!wait_bar(bar.kv_empty(st), par ^ 1, g, kStatusTimeoutLoad)) {
-        ok = false;
-        break;
+        tma_load_3d(base + C::OFF_Q + t * C::Q_TILE + r * C::Q_REGION, tm_q, bar.q_full(t), r * C::RC,
+                    x.row0 + t * C::BQ, x.bh, pol_q);
+      last_q[t] = qi;
+    }
+    return true;
+  };
+  // Next free stage: waits for its previous contents to be released; returns
+  // its shared address in s0 and arms kv_full for `tiles` tiles.
+  auto stage_begin = [&](int tiles, uint32_t& s0, uint32_t& full) -> bool {
+    const int st = pos % C::NST;
+    const uint32_t par = (pos / C::NST) & 1;
+    if (!wait_bar(bar.kv_empty(st), par ^ 1, g, kStatusTimeoutLoad)) return false;
+    s0 = base + C::OFF_KV + st * C::STAGE;
+    full = bar.kv_full(st);
+    mbar_arrive_expect_tx(full, tiles * C::KV_TILE);
+    issued |= 1u << st;
+    last_par = (last_par & ~(1u << st)) | (par << st);
+    ++pos;
+    return true;
+  };
+
+  if constexpr (C::NQT == 2) {
+    int uk = 0;
+    int u = tc_unit(0);
+    if (u < p.total_units) {
+      TcUnit w = tc_decode<D, CAUSAL>(u, p);
+      uint32_t s0, full;
+      ok = load_q(w, 0) && stage_begin(1, s0, full);
+      if (ok) load_tile(tm_k, s0, full, 0, w.bh);
+      while (ok) {
+        const int un = tc_unit(uk + 1);
+        const bool has_next = un < p.total_units;
+        const TcUnit wn = tc_decode<D, CAUSAL>(has_next ? un : u, p);
+        for (int j = 0; ok && j < w.nmax; ++j) {
+          const bool k_here = j + 1 < w.nmax;
+          const bool k_next = !k_here && has_next;
+          if (!(ok = stage_begin((k_here || k_next) ? 2 : 1, s0, full))) break;
+          load_tile(tm_v, s0, full, j, w.bh);
+          if (k_here) load_tile(tm_k, s0 + C::KV_TILE, full, j + 1, w.bh);
+          if (k_next) load_tile(tm_k, s0 + C::KV_TILE, full, 0, wn.bh);
+        }
+        if (!ok || !has_next) break;
+        ++uk;
+        ok = load_q(wn, uk);
+        u = un;
+        w = wn;
       }
-      const uint32_t s0 = base + C::OFF_KV + st * C::STAGE;
-      if (t < 0) {  // K_0 .. K_{LA-1}
-        const int nk = C::LA < w.nmax ? C::LA : w.nmax;
-        mbar_arrive_expect_tx(bar.kv_full(st), nk * C::KV_TILE);
-        for (int k = 0; k < nk; ++k) load_tile(tm_k, s0 + k * C::KV_TILE, bar.kv_full(st), k, w.bh);
-      } else {  // V_t, K_{t+LA}
-        const bool has_k = t + C::LA < w.nmax;
-        mbar_arrive_expect_tx(bar.kv_full(st), (has_k ? 2 : 1) * C::KV_TILE);
-        load_tile(tm_v, s0, bar.kv_full(st), t, w.bh);
-        if (has_k) load_tile(tm_k, s0 + C::KV_TILE, bar.kv_full(st), t + C::LA, w.bh);
+    }
+  } else {
+    for (int uk = 0, u; ok && (u = tc_unit(uk)) < p.total_units; ++uk) {
+      const TcUnit w = tc_decode<D, CAUSAL>(u, p);
+      if (!(ok = load_q(w, uk))) break;
+      uint32_t s0, full;
+      for (int t = -1; t < w.nmax; ++t) {
+        if (t < 0) {  // K_0 .. K_{LA-1}
+          const int nk = C::LA < w.nmax ? C::LA : w.nmax;
+          if (!(ok = stage_begin(nk, s0, full))) break;
+          for (int k = 0; k < nk; ++k) load_tile(tm_k, s0 + k * C::KV_TILE, full, k, w.bh);
+        } else {  // V_t, K_{t+LA}
+          const bool has_k = t + C::LA < w.nmax;
+          if (!(ok = stage_begin(has_k ? 2 : 1, s0, full))) break;
+          load_tile(tm_v, s0, full, t, w.bh);
+          if (has_k) load_tile(tm_k, s0 + C::KV_TILE, full, t + C::LA, w.bh);
+        }
       }
-      issued |= 1u << st;
-      last_par = (last_par & ~(1u << st)) | (par << st);
-      ++pos;
     }
   }
   // Every issued copy must land before the CTA may exit.
   for (int i = 0; i < C::NST; ++i)
     if (issued & (1u << i)) wait_bar_drain(bar.kv_full(i), (last_par >> i) & 1, g);
-  if (last_q >= 0) wait_bar_drain(bar.q_full(), last_q & 1, g);
+  for (int t = 0; t < C::NQT; ++t)
+    if (last_q[t] >= 0) wait_bar_drain(bar.q_full(t), last_q[t] & 1, g);
 }
 
 // ------------------------------------------------------------------ MMA issuer
@@ -343,15 +393,14 @@ __device__ __forceinline__ void tc_mma(const TcParams& p, const TcBars<D>& bar, 
   };
   uint32_t pos = 0;               // K/V stages consumed
   uint32_t go0 = 0, go1 = 0;      // pv_go phases consumed, per O accumulator
-  uint32_t qk_total = 0;          // single-tile mode: S products issued so far
   bool ok = true;
-  int ui = 0;
 
   // Acquire the next K/V stage; its tiles sit at positions 2*st and 2*st + 1.
   auto stage_acquire = [&](uint32_t& st) -> bool {
     st = pos % C::NST;
     const bool r = wait(bar.kv_full(st), (pos / C::NST) & 1);
     ++pos;
+    if (r) tc_fence_after();
     return r;
   };
   auto pv_wait = [&](int t, uint32_t& go) -> bool {
@@ -362,42 +411,76 @@ __device__ __forceinline__ void tc_mma(const TcParams& p, const TcBars<D>& bar, 
     return true;
   };
 
-  for (int uk = 0, u; ok && (u = tc_unit(uk)) < p.total_units; ++uk, ++ui) {
-    const TcUnit w = tc_decode<D, CAUSAL>(u, p);
-    if (!wait(bar.q_full(), ui & 1)) {
-      ok = false;
-      break;
-    }
-    uint32_t st;
-    if (!(ok = stage_acquire(st))) break;
-    tc_fence_after();
-    if constexpr (C::NQT == 2) {
-      // First stage: K_0.
-      if (w.n[0] > 0) M.qk(0, 0, 2 * st, bar.s_full(0));
-      if (w.n[1] > 0) M.qk(1, 1, 2 * st, bar.s_full(1));
-      M.commit(bar.kv_empty(st));
-      if (w.nmax == 1) M.commit(bar.q_empty());
-      for (int j = 0; j < w.nmax; ++j) {
-        // Stage j: V_j at position 2*st, K_{j+1} at 2*st + 1.
-        if (!(ok = stage_acquire(st))) break;
-        // query tile 0: P V j, then S for key tile j+1
-        if (j < w.n[0]) {
-          if (!(ok = pv_wait(0, go0))) break;
-          M.pv(0, 0, 2 * st, j > 0);
-          if (j == w.n[0] - 1) M.commit(bar.o_done(0));
-        }
-        if (j + 1 < w.n[0]) M.qk(0, 0, 2 * st + 1, bar.s_full(0));
-        // query tile 1
-        if (j < w.n[1]) {
-          if (!(ok = pv_wait(1, go1))) break;
-          M.pv(1, 1, 2 * st, j > 0);
-          if (j == w.n[1] - 1) M.commit(bar.o_done(1));
-        }
-        if (j + 1 < w.n[1]) M.qk(1, 1, 2 * st + 1, bar.s_full(1));
-        M.commit(bar.kv_empty(st));
-        if (j + 1 == w.nmax - 1) M.commit(bar.q_empty());
+  if constexpr (C::NQT == 2) {
+    // One continuous stream over the CTA's units (see the producer).  Per
+    // step j of unit w, tile t: P V_t j, then S_t for key tile j + 1, or, in
+    // the unit's last step, S_t for key tile 0 of the next unit, whose Q_t
+    // has been loaded meanwhile.  Q_t of a unit is released after its last
+    // S_t product.  The next unit's first products still wait for O_t to be
+    // read out by the epilogue (there is no room in TMEM for a second O).
+    int uk = 0;
+    int u = tc_unit(0);
+    // S_t for key tile 0 of unit x (the qi-th unit), K_0 at position kpos.
+    auto first_qk = [&](const TcUnit& x, int qi, int t, uint32_t kpos) -> bool {
+      if (!wait(bar.q_full(t), qi & 1)) return false;
+      tc_fence_after();
+      if (x.n[t] > 0) M.qk(t, t, kpos, bar.s_full(t));
+      if (x.n[t] <= 1) M.commit(bar.q_empty(t));
+      return true;
+    };
+    // Step j of unit w for tile t, with the stage at st: P V_t j ...
+    auto tile_pv = [&](const TcUnit& w, int j, int t, uint32_t st, uint32_t& go) -> bool {
+      if (j < w.n[t]) {
+        if (!pv_wait(t, go)) return false;
+        M.pv(t, t, 2 * st, j > 0);
+        if (j == w.n[t] - 1) M.commit(bar.o_done(t));
       }
-    } else {
+      return true;
+    };
+    // ... then S_t for key tile j + 1, or key tile 0 of the next unit.
+    auto tile_qk = [&](const TcUnit& w, int j, int t, uint32_t st, bool has_next, const TcUnit& wn, int qn) -> bool {
+      if (j + 1 < w.n[t]) {
+        M.qk(t, t, 2 * st + 1, bar.s_full(t));
+        if (j + 1 == w.n[t] - 1) M.commit(bar.q_empty(t));
+      } else if (j == w.nmax - 1 && has_next) {
+        return first_qk(wn, qn, t, 2 * st + 1);
+      }
+      return true;
+    };
+    if (u < p.total_units) {
+      TcUnit w = tc_decode<D, CAUSAL>(u, p);
+      uint32_t st;
+      ok = stage_acquire(st) && first_qk(w, 0, 0, 2 * st) && first_qk(w, 0, 1, 2 * st);
+      if (ok) M.commit(bar.kv_empty(st));
+      while (ok) {
+        const int un = tc_unit(uk + 1);
+        const bool has_next = un < p.total_units;
+        const TcUnit wn = tc_decode<D, CAUSAL>(has_next ? un : u, p);
+        for (int j = 0; ok && j < w.nmax; ++j) {
+          if (!(ok = stage_acquire(st))) break;
+          // In a unit's last step both P V products go first: the next unit's
+          // S products may have to wait for its Q tiles.
+          if (j == w.nmax - 1)
+            ok = tile_pv(w, j, 0, st, go0) && tile_pv(w, j, 1, st, go1) &&
+                 tile_qk(w, j, 0, st, has_next, wn, uk + 1) && tile_qk(w, j, 1, st, has_next, wn, uk + 1);
+          else
+            ok = tile_pv(w, j, 0, st, go0) && tile_qk(w, j, 0, st, has_next, wn, uk + 1) &&
+                 tile_pv(w, j, 1, st, go1) && tile_qk(w, j, 1, st, has_next, wn, uk + 1);
+          if (ok) M.commit(bar.kv_empty(st));
+        }
+        if (!ok || !has_next) break;
+        ++uk;
+        u = un;
+        w = wn;
+      }
+    }
+  } else {
+    uint32_t qk_total = 0;  // S products issued so far
+    for (int uk = 0, u; ok && (u = tc_unit(uk)) < p.total_units; ++uk) {
+      const TcUnit w = tc_decode<D, CAUSAL>(u, p);
+      if (!(ok = wait(bar.q_full(0), uk & 1))) break;
+      uint32_t st;
+      if (!(ok = stage_acquire(st))) break;
       const int n = w.n[0];
       const uint32_t qk_base = qk_total;  // S product of key tile j sits in buffer (qk_base + j) & 1
       // First stage: K_0, K_1.
@@ -406,7 +489,7 @@ __device__ __forceinline__ void tc_mma(const TcParams& p, const TcBars<D>& bar, 
         ++qk_total;
       }
       M.commit(bar.kv_empty(st));
-      if (n <= C::LA) M.commit(bar.q_empty());
+      if (n <= C::LA) M.commit(bar.q_empty(0));
       for (int j = 0; j < n; ++j) {
         // Stage j: V_j at 2*st, K_{j+2} at 2*st + 1.
         if (!(ok = stage_acquire(st))) break;
@@ -416,7 +499,7 @@ __device__ __forceinline__ void tc_mma(const TcParams& p, const TcBars<D>& bar, 
         if (j + C::LA < n) {
           M.qk(0, qk_total & 1, 2 * st + 1, bar.s_full(qk_total & 1));
           ++qk_total;
-          if (j + C::LA == n - 1) M.commit(bar.q_empty());
+          if (j + C::LA == n - 1) M.commit(bar.q_empty(0));
         }
         M.commit(bar.kv_empty(st));
       }
@@ -537,8 +620,8 @@ __device__ __forceinline__ void tc_softmax(const TcParams& p, const TcBars<D>& b
       warp_arrive(C::NQT == 2 ? bar.pv_go(ot, 0) : bar.pv_go(0, (s_waits - 1) & 1));
     }
     if (!ok) break;
-    stat_m[r] = m;
-    stat_l[r] = l;
+    stat_m[(uk & 1) * 256 + r] = m;
+    stat_l[(uk & 1) * 256 + r] = l;
     warp_arrive(bar.l_full(ot));
   }
 }
@@ -604,15 +687,15 @@ __device__ __forceinline__ void tc_correction(const TcParams& p, const TcBars<D>
     return true;
   };
   // Epilogue of accumulator t: O / l in bf16, L = (m + log2 l) * ln 2; then O is free again.
-  auto epilogue = [&](const TcUnit& w, int t, uint32_t& od, uint32_t& lf) -> bool {
+  auto epilogue = [&](const TcUnit& w, int su, int t, uint32_t& od, uint32_t& lf) -> bool {
     bool k = warp_wait_bar(bar.o_done(t), od & 1, g, kStatusTimeoutSoftmax);
     k = k && warp_wait_bar(bar.l_full(t), lf & 1, g, kStatusTimeoutSoftmax);
     if (!k) return false;
     ++od;
     ++lf;
     tc_fence_after();
-    const float mrow = stat_m[t * 128 + r];
-    const float lrow = stat_l[t * 128 + r];
+    const float mrow = stat_m[su * 256 + t * 128 + r];
+    const float lrow = stat_l[su * 256 + t * 128 + r];
     const float inv_l = 1.f / lrow;
     const uint64_t il2 = f2_pack(inv_l, inv_l);
     const int row = w.row0 + t * C::BQ + r;
@@ -651,8 +734,8 @@ __device__ __forceinline__ void tc_correction(const TcParams& p, const TcBars<D>
     for (int j = 0; ok && j < w.nmax; ++j) {
       if (ok && j >= 1 && j < w.n[0]) ok = rescale(0, a_cnt0, od0);
       if (C::NO == 2 && ok && j >= 1 && j < w.n[1]) ok = rescale(1, a_cnt1, od1);
-      if (ok && j == w.n[0] - 1) ok = epilogue(w, 0, od0, lf0);
-      if (C::NO == 2 && ok && j == w.n[1] - 1) ok = epilogue(w, 1, od1, lf1);
+      if (ok && j == w.n[0] - 1) ok = epilogue(w, uk & 1, 0, od0, lf0);
+      if (C::NO == 2 && ok && j == w.n[1] - 1) ok = epilogue(w, uk & 1, 1, od1, lf1);
     }
   }
 }
@@ -674,8 +757,10 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::OFF_ABORT);
 
   if (threadIdx.x == 0) {
-    mbar_init(bar.q_full(), 1);
-    mbar_init(bar.q_empty(), 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar.q_full(t), 1);
+      mbar_init(bar.q_empty(t), 1);
+    }
     for (int i = 0; i < C::NST; ++i) {
       mbar_init(bar.kv_full(i), 1);
       mbar_init(bar.kv_empty(i), 1);
