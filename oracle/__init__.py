@@ -1,8 +1,10 @@
-"""fp64 CPU oracle for the attention forward pass.
+"""fp64 CPU oracle for the attention forward and backward passes.
 
 TEST INFRASTRUCTURE ONLY: imported by tests, by the smoke check and by the
 benchmark's CPU-baseline and reference legs, never by the product path.
 """
 from .attention import attention, attention_head, logsumexp_rows, probabilities, scores
+from .backward import attention_backward, attention_backward_head
 
-__all__ = ["attention", "attention_head", "logsumexp_rows", "probabilities", "scores"]
+__all__ = ["attention", "attention_head", "logsumexp_rows", "probabilities", "scores",
+           "attention_backward", "attention_backward_head"]
