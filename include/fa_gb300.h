@@ -53,7 +53,7 @@ enum {
   FA_ERR_TIMEOUT = -6,        /* a bounded device-side wait expired (reported by fa_status)  */
   FA_ERR_ARCH = -7,           /* the current device is not a compute capability 10.3 GPU     */
   FA_ERR_BAD_SCALE = -8,      /* scale is not a finite number > 0                            */
-  FA_ERR_WORKSPACE = -9,      /* the workspace passed to fa_fwd_host is too small            */
+  FA_ERR_WORKSPACE = -9,      /* the workspace passed to fa_fwd_host or fa_bwd is too small  */
   FA_ERR_SCRATCH = -10        /* the kernel needs more scratch than fa_fwd_noalloc provides  */
 };
 
@@ -108,6 +108,40 @@ size_t fa_fwd_host_workspace_bytes(int B, int H, int N, int d);
 int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse,
                 void* workspace, size_t workspace_bytes,
                 int B, int H, int N, int d, float scale, int causal, void* stream);
+
+/*
+ * fa_bwd_workspace_bytes - size of the device workspace fa_bwd needs: two fp32
+ * vectors of B*H*round_up(N, 64) rows (L * log2(e) and D = rowsum(dO * O)),
+ * each 256-byte aligned.  Returns 0 for invalid shapes.
+ */
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * fa_bwd - bf16 backward pass on the tensor cores: the gradients of
+ * O = softmax(Q K^T * scale) V (causal mask optional) with respect to Q, K, V
+ * given the upstream gradient dO.  P is recomputed from the forward's L as
+ * exp(scale * Q K^T - L) ("FlashAttention-2 from PyTorch to Triton", "What We
+ * Are Building"); as in the metal-flash-attention backward ("Case Study:
+ * metal-flash-attention") a dK/dV kernel and a dQ kernel each own their
+ * outputs, so the results are deterministic (no atomics).  Three kernels are
+ * enqueued on `stream`: D = rowsum(dO * O), dK/dV, dQ.
+ *
+ *   q, k, v, o, dout : device pointers to bf16 [B][H][N][d], 16-byte aligned;
+ *                      o and lse are the outputs of fa_fwd for q, k, v, scale, causal.
+ *   lse              : device pointer to fp32 [B][H][N].
+ *   dq, dk, dv       : device pointers to bf16 [B][H][N][d], 16-byte aligned; fully overwritten.
+ *   d                : head dimension, one of 32, 64, 128 (else FA_ERR_UNSUPPORTED_D).
+ *   workspace        : device pointer, 256-byte aligned, at least fa_bwd_workspace_bytes(B, H, N, d)
+ *                      bytes (else FA_ERR_WORKSPACE); its contents on entry are ignored.
+ *   Other arguments and behaviour as fa_fwd.
+ *
+ * Arithmetic: bf16 products with fp32 accumulation; P and dS are rounded to
+ * bf16 before they enter the dV, dK and dQ products; D in fp32; dQ and dK
+ * carry the factor `scale`; outputs rounded to bf16 once at the end.
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+           void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
+           void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * fa_fwd_noalloc - fa_fwd for callers that must not allocate device memory.

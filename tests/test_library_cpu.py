@@ -115,3 +115,32 @@ def test_tensor_core_kernels_fit_their_register_split():
             assert r["registers"] == 128, (name, r)
         else:
             assert r["registers"] <= 168, (name, r)
+
+
+def test_backward_workspace_size_and_host_checks(lib):
+    r256 = lambda x: (x + 255) // 256 * 256
+    n = fa.fa_bwd_workspace_bytes(2, 3, 100, 64)
+    assert n == 2 * r256(2 * 3 * 128 * 4)  # N padded to a multiple of 64
+    assert fa.fa_bwd_workspace_bytes(2, 3, 0, 64) == 0
+    ws = FAKE * 16
+    common = (2, 3, 100, 64, 0.125, 0)
+    ptrs = [FAKE] * 9
+    assert fa.fa_bwd(*ptrs, *common, ws, n - 1, None) == -9            # workspace too small
+    assert fa.fa_bwd(*ptrs, *common, FAKE + 16, n, None) == -4         # workspace not 256-byte aligned
+    assert fa.fa_bwd(*ptrs, *common, 0, n, None) == -1                 # workspace missing
+    assert fa.fa_bwd(*ptrs[:5], 0, *ptrs[6:], *common, ws, n, None) == -1   # dO missing
+    assert fa.fa_bwd(*ptrs, 2, 3, 100, 256, 0.125, 0, ws, n, None) == -3    # no d = 256 backward
+    assert fa.fa_bwd(*ptrs, 2, 3, 100, 64, -1.0, 0, ws, n, None) == -8
+    bad = list(ptrs)
+    bad[6] = FAKE + 8
+    assert fa.fa_bwd(*bad, *common, ws, n, None) == -4                 # dq not 16-byte aligned
+
+
+def test_backward_kernels_do_not_spill():
+    if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+        pytest.skip("nvcc not available")
+    rep = build.ptxas_report({"fa_bwd_d32.cu", "fa_bwd_d64.cu", "fa_bwd_d128.cu"})
+    ks = {k: v for k, v in rep.items() if "fa_bwd" in k}
+    assert len(ks) == 15  # per head dimension: 4 tensor-core kernels and 1 preprocessing kernel
+    for name, r in ks.items():
+        assert r["spill_stores"] == 0 and r["spill_loads"] == 0, (name, r)

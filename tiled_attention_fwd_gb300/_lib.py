@@ -1,6 +1,6 @@
 """ctypes binding of libfa_gb300.so: the C ABI with the same names, and a
-torch-tensor convenience wrapper.  Argument marshalling only: every step of
-the forward pass runs in the library's CUDA kernels.  There is no fallback:
+torch-tensor convenience wrappers.  Argument marshalling only: every step of
+the forward and backward passes runs in the library's CUDA kernels.  There is no fallback:
 if the library is missing or fails to load, every call raises.
 """
 from __future__ import annotations
@@ -25,6 +25,8 @@ _SIGNATURES = {
     "fa_fwd_host_workspace_bytes": (_c_size_t, [_c_int] * 4),
     "fa_fwd_host": (_c_int, [_c_void_p] * 6 + [_c_size_t] + [_c_int] * 4 + [_c_float, _c_int, _c_void_p]),
     "fa_fwd_noalloc": (_c_int, [_c_void_p] * 5 + [_c_int] * 4 + [_c_float, _c_int, _c_void_p]),
+    "fa_bwd_workspace_bytes": (_c_size_t, [_c_int] * 4),
+    "fa_bwd": (_c_int, [_c_void_p] * 9 + [_c_int] * 4 + [_c_float, _c_int, _c_void_p, _c_size_t, _c_void_p]),
     "fa_status": (_c_int, [_c_void_p]),
     "fa_set_wait_limit_ms": (_c_int, [_c_int]),
     "fa_strerror": (ctypes.c_char_p, [_c_int]),
@@ -105,6 +107,17 @@ def fa_fwd_noalloc(q, k, v, o, lse, B, H, N, d, scale, causal, stream) -> int:
     return load().fa_fwd_noalloc(q, k, v, o, lse, B, H, N, d, scale, int(bool(causal)), stream)
 
 
+def fa_bwd_workspace_bytes(B, H, N, d) -> int:
+    return load().fa_bwd_workspace_bytes(B, H, N, d)
+
+
+def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal, workspace, workspace_bytes,
+           stream) -> int:
+    """bf16 tensor-core backward; pointers are integers (device addresses)."""
+    return load().fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, int(bool(causal)), workspace,
+                         workspace_bytes, stream)
+
+
 def fa_status(stream) -> int:
     return load().fa_status(stream)
 
@@ -155,6 +168,40 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
                 float(scale), causal, stream)
     _check(rc, fn.__name__)
     return o, l
+
+
+def backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None, workspace=None):
+    """dQ, dK, dV of the attention forward for bf16 CUDA tensors [B, H, N, d].
+
+    ``o`` and ``lse`` are the outputs of ``forward`` for the same q, k, v,
+    causal and scale; ``dout`` is the upstream gradient.  ``workspace`` (a
+    CUDA uint8 tensor of at least fa_bwd_workspace_bytes, 256-byte aligned) is
+    allocated here if not given.  Returns (dQ, dK, dV) in bf16.  Enqueued on
+    the current stream.
+    """
+    import torch
+
+    ts = (q, k, v, o, dout)
+    if q.dim() != 4 or any(t.shape != q.shape for t in ts):
+        raise ValueError("q, k, v, o, dout must share the shape [B, H, N, d]")
+    if not all(t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous() for t in ts):
+        raise ValueError("q, k, v, o, dout must be contiguous bf16 CUDA tensors")
+    B, H, N, d = q.shape
+    if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_cuda:
+        raise ValueError("lse must be an fp32 CUDA tensor [B, H, N]")
+    if scale is None:
+        scale = d ** -0.5
+    need = fa_bwd_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    with torch.cuda.device(q.device):
+        rc = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
+                    dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, float(scale), causal,
+                    workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                    _stream_handle(torch, q.device))
+    _check(rc, "fa_bwd")
+    return dq, dk, dv
 
 
 def check_status(device=None):

@@ -201,6 +201,55 @@ int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse
   return FA_OK;
 }
 
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
+  const size_t n_pad = (static_cast<size_t>(N) + 63) / 64 * 64;
+  return 2 * fa::round256(static_cast<size_t>(B) * H * n_pad * 4);
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout, void* dq,
+           void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, void* workspace,
+           size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace) return FA_ERR_NULL_POINTER;
+  int rc = fa::check_common(B, H, N, d, scale);
+  if (rc != FA_OK) return rc;
+  if (d != 32 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED_D;
+  if (!fa::aligned16(q) || !fa::aligned16(k) || !fa::aligned16(v) || !fa::aligned16(o) || !fa::aligned16(dout) ||
+      !fa::aligned16(dq) || !fa::aligned16(dk) || !fa::aligned16(dv) || (reinterpret_cast<uintptr_t>(lse) & 3u) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return FA_ERR_MISALIGNED;
+  if (workspace_bytes < fa_bwd_workspace_bytes(B, H, N, d)) return FA_ERR_WORKSPACE;
+  fa::DeviceState* s = nullptr;
+  rc = fa::current_device_state(&s);
+  if (rc != FA_OK) return rc;
+  const fa::LaunchCtx ctx = fa::make_ctx(*s, stream);
+  fa::BwdArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.dout = dout;
+  a.lse = lse;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.BH = B * H;
+  a.N = N;
+  a.n_pad = (N + 63) / 64 * 64;
+  a.scale = scale;
+  a.causal = causal != 0;
+  a.l2 = static_cast<float*>(workspace);
+  a.dsum = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                    fa::round256(static_cast<size_t>(a.BH) * a.n_pad * 4));
+  int e = 0;
+  switch (d) {
+    case 32: e = fa::launch_bwd_d32(a, ctx); break;
+    case 64: e = fa::launch_bwd_d64(a, ctx); break;
+    default: e = fa::launch_bwd_d128(a, ctx); break;
+  }
+  return e == 0 ? FA_OK : FA_ERR_CUDA;
+}
+
 int fa_status(void* stream) {
   fa::DeviceState* s = nullptr;
   int rc = fa::current_device_state(&s);

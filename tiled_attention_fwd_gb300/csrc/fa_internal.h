@@ -41,6 +41,33 @@ int launch_tc_d128(bool causal, const void* q, const void* k, const void* v, voi
 int launch_tc_d256(bool causal, const void* q, const void* k, const void* v, void* o, float* lse, int BH, int N,
                    float scale, const LaunchCtx& ctx);
 
+// Arguments of the backward pass (device pointers; bf16 tensors [BH][N][d],
+// lse fp32 [BH][N]; l2 and dsum are workspace vectors [BH][n_pad]).
+struct BwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const void* dout;
+  const float* lse;
+  void* dq;
+  void* dk;
+  void* dv;
+  int BH;
+  int N;
+  int n_pad;       // N rounded up to a multiple of 64
+  float scale;
+  bool causal;
+  float* l2;
+  float* dsum;
+};
+
+// bf16 tensor-core backward (preprocessing, dK/dV kernel, dQ kernel) for one
+// head dimension; returns a cudaError_t-like code.  Defined in fa_bwd_d<D>.cu.
+int launch_bwd_d32(const BwdArgs& a, const LaunchCtx& ctx);
+int launch_bwd_d64(const BwdArgs& a, const LaunchCtx& ctx);
+int launch_bwd_d128(const BwdArgs& a, const LaunchCtx& ctx);
+
 // fp32 SIMT forward, 1 <= d <= 256.  Defined in fa_simt.cu.
 int launch_simt(bool causal, const float* q, const float* k, const float* v, float* o, float* lse, int BH, int N,
                 int d, float scale, const LaunchCtx& ctx);

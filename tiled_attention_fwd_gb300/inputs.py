@@ -94,6 +94,15 @@ def make_qkv(w: Workload):
     return q.to(dt).contiguous(), k.to(dt).contiguous(), v.to(dt).contiguous()
 
 
+def make_dout(w: Workload):
+    """Upstream gradient dO for the backward pass of workload ``w``: N(0, 1) in
+    w.dtype, drawn from its own generator (seed w.seed + 1000) so that Q, K, V
+    are the same as for the forward pass."""
+    g = torch.Generator(device="cpu").manual_seed(w.seed + 1000)
+    do = torch.randn((w.B, w.H, w.N, w.d), generator=g, dtype=torch.float32)
+    return do.to(w.torch_dtype).contiguous()
+
+
 def as_f64_numpy(t: torch.Tensor):
     """Widen an (already rounded) CPU tensor to an fp64 numpy array."""
     return t.detach().to("cpu", torch.float64).numpy()
