@@ -8,6 +8,10 @@ in HBM.  Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
+With --pass bwd a step is one backward pass instead (fa_bwd: D = rowsum(dO*O),
+the dK/dV kernel and the dQ kernel, with Q, K, V, O, L and dO resident), and
+the line reports TFLOP/s over 2.5x the forward's algorithmic FLOPs.
+
 Under torchrun (N > 1) every rank runs the same workload on its own GPU
 (independent replicas: the path needs no exchange between GPUs), the timed
 region is bracketed by a barrier and a synchronize on both sides, the time
@@ -39,17 +43,21 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "FA2 fwd TFLOP/s, bf16 B4 H16 N4096 d128 causal; % of GB300 dense peak"
+BWD_METRIC = "FA2 bwd TFLOP/s (2.5x the forward's algorithmic FLOPs), bf16; % of GB300 dense peak"
+BWD_FLOP_FACTOR = 2.5  # dV = P^T dO, dP = dO V^T, dQ = dS K, dK = dS^T Q, plus S = Q K^T recomputed
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20  # larger than the 129 MB L2
 KERNEL_SOURCES = ["tiled_attention_fwd_gb300/csrc/fa_fwd_tc.cuh", "tiled_attention_fwd_gb300/csrc/ptx.cuh",
                   "tiled_attention_fwd_gb300/csrc/fa_tc_launch.cuh"]
+BWD_KERNEL_SOURCES = ["tiled_attention_fwd_gb300/csrc/fa_bwd_tc.cuh", "tiled_attention_fwd_gb300/csrc/ptx.cuh",
+                      "tiled_attention_fwd_gb300/csrc/fa_bwd_launch.cuh"]
 
 
 # ------------------------------------------------------------------ helpers
-def kernel_source_hash() -> str:
+def kernel_source_hash(sources=None) -> str:
     h = hashlib.sha256()
-    for p in KERNEL_SOURCES:
+    for p in (KERNEL_SOURCES if sources is None else sources):
         with open(os.path.join(ROOT, p), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -64,14 +72,14 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def load_traffic(workload: str):
+def load_traffic(workload: str, prefix: str = "traffic", sources=None):
     """dram bytes per launch from a committed ncu summary, if it was taken on this kernel source."""
-    path = os.path.join(ROOT, "profiles", f"traffic_{workload}.json")
+    path = os.path.join(ROOT, "profiles", f"{prefix}_{workload}.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
-    if d.get("kernel_source_hash") != kernel_source_hash():
+    if d.get("kernel_source_hash") != kernel_source_hash(sources):
         return None
     return d.get("dram_bytes_per_launch")
 
@@ -162,19 +170,31 @@ def _oracle_head(args):
     return time.perf_counter() - t0
 
 
-def oracle_sample(w, budget_s: float, pool, cores: int, inputs=None):
-    """Run the fp64 oracle on whole heads of workload `w` for about `budget_s`
-    seconds on `cores` worker processes; returns (TFLOP/s, heads, seconds)."""
-    from tiled_attention_fwd_gb300.inputs import as_f64_numpy, make_qkv
+def _oracle_bwd_head(args):
+    import oracle
+    q, k, v, do, scale, causal = args
+    t0 = time.perf_counter()
+    oracle.attention_backward_head(q, k, v, do, scale, causal)
+    return time.perf_counter() - t0
+
+
+def oracle_sample(w, budget_s: float, pool, cores: int, inputs=None, backward=False):
+    """Run the fp64 oracle (forward, or backward given dO) on whole heads of
+    workload `w` for about `budget_s` seconds on `cores` worker processes;
+    returns (TFLOP/s, heads, seconds), counting the algorithmic FLOPs."""
+    from tiled_attention_fwd_gb300.inputs import as_f64_numpy, make_dout, make_qkv
 
     q, k, v = make_qkv(w) if inputs is None else inputs
     heads = [(b, h) for b in range(w.B) for h in range(w.H)]
-    per_head = w.flops / len(heads)
+    per_head = w.flops / len(heads) * (BWD_FLOP_FACTOR if backward else 1.0)
     qn, kn, vn = as_f64_numpy(q), as_f64_numpy(k), as_f64_numpy(v)
+    don = as_f64_numpy(make_dout(w)) if backward else None
     t0 = time.perf_counter()
 
     def submit(i):
         b, h = heads[i]
+        if backward:
+            return pool.apply_async(_oracle_bwd_head, ((qn[b, h], kn[b, h], vn[b, h], don[b, h], w.scale, w.causal),))
         return pool.apply_async(_oracle_head, ((qn[b, h], kn[b, h], vn[b, h], w.scale, w.causal),))
 
     pending = [submit(i) for i in range(min(cores, len(heads)))]
@@ -205,21 +225,24 @@ def run_reference(args, w):
     cores = os.cpu_count() or 1
     pool = make_pool(cores)
     inputs = make_qkv(w)
+    bwd = args.pass_ == "bwd"
     budget = max(2.0, 60.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
-        oracle_sample(w, budget, pool, cores, inputs)
+        oracle_sample(w, budget, pool, cores, inputs, backward=bwd)
     vals, heads, secs = [], 0, 0.0
     for _ in range(args.steps):
-        v, h, s = oracle_sample(w, budget, pool, cores, inputs)
+        v, h, s = oracle_sample(w, budget, pool, cores, inputs, backward=bwd)
         vals.append(v)
         heads += h
         secs += s
     pool.close()
-    value = heads * (w.flops / (w.B * w.H)) / secs / 1e12
+    value = heads * (w.flops / (w.B * w.H)) * (BWD_FLOP_FACTOR if bwd else 1.0) / secs / 1e12
     sample = (f"whole heads of the workload, as many as fit in ~{budget:.0f} s per step on {cores} worker "
-              f"processes (one head each, fp64, BLAS single-threaded); {heads} heads in {args.steps} steps")
+              f"processes (one head each, fp64 {'backward' if bwd else 'forward'}, BLAS single-threaded); "
+              f"{heads} heads in {args.steps} steps")
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "impl": "reference", "metric": BWD_METRIC if bwd else METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": secs / max(1, args.steps) * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_of(w),
@@ -368,6 +391,149 @@ def run_ours(args, w):
     return 0
 
 
+def run_ours_bwd(args, w):
+    """The backward pass (fa_bwd: preprocessing + dK/dV + dQ kernels) of workload `w`."""
+    import torch
+    import torch.distributed as dist
+
+    import tiled_attention_fwd_gb300 as fa
+    from tiled_attention_fwd_gb300.inputs import make_dout, make_qkv
+
+    if w.dtype != "bf16" or w.d not in (32, 64, 128):
+        raise SystemExit(f"the backward pass covers bf16 with d in (32, 64, 128), not {w.name}")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    want_cpu = (not args.no_cpu_baseline) and rank == 0 and world == 1
+    cores = os.cpu_count() or 1
+    pool = make_pool(cores) if want_cpu else None  # spawn before the first GPU call
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    reduce_max = None
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+        reduce_max = make_reduce_max(dist, dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    q, k, v = make_qkv(w)
+    do = make_dout(w)
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o, lse = fa.forward(qd, kd, vd, causal=w.causal, scale=w.scale)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    nws = fa.fa_bwd_workspace_bytes(w.B, w.H, w.N, w.d)
+    ws = torch.empty(nws, dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    flops = BWD_FLOP_FACTOR * w.flops
+
+    def step():
+        rc = fa.fa_bwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), lse.data_ptr(), dod.data_ptr(),
+                       dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), w.B, w.H, w.N, w.d, w.scale, w.causal,
+                       ws.data_ptr(), nws, sh)
+        if rc != 0:
+            raise fa.FAError(rc, "fa_bwd")
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    fa.check_status(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local) as clocks:
+        barrier()
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        barrier()
+        t_wall = time.perf_counter() - t_wall
+    fa.check_status(dev)
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    total_s = aggregate_ranks(sum(step_ms) / 1e3, world, reduce_max)
+    value = job_throughput(world, args.steps, flops, total_s)
+    kernel_ms = statistics.mean(step_ms)
+
+    # End to end through the public Python API on HOST tensors: copies of Q, K,
+    # V, O, L and dO from pinned memory, backward(), copies of dQ, dK, dV back.
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv, hdo = (t.pin_memory() for t in (q, k, v, do))
+        ho, hl = o.cpu().pin_memory(), lse.cpu().pin_memory()
+        outs = [torch.empty_like(hq).pin_memory() for _ in range(3)]
+        dev_in = [torch.empty_like(qd) for _ in range(5)]
+        dev_l = torch.empty_like(lse)
+
+        def host_step():
+            for src, dst in zip((hq, hk, hv, ho, hdo), dev_in):
+                dst.copy_(src, non_blocking=True)
+            dev_l.copy_(hl, non_blocking=True)
+            grads = fa.backward(*dev_in[:4], dev_l, dev_in[4], causal=w.causal, scale=w.scale, workspace=ws)
+            for src, dst in zip(grads, outs):
+                dst.copy_(src, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            host_step()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            host_step()
+        e1.record(stream)
+        barrier()
+        e2e_s = aggregate_ranks(e0.elapsed_time(e1) / 1e3, world, reduce_max)
+        tb = w.B * w.H * w.N * w.d * 2
+        e2e = {"value": job_throughput(world, args.steps, flops, e2e_s), "unit": UNIT,
+               "h2d_bytes_per_step": 5 * tb + w.B * w.H * w.N * 4, "d2h_bytes_per_step": 3 * tb,
+               "ms_per_step": e2e_s / args.steps * 1e3, "api": "tiled_attention_fwd_gb300.backward (pinned host tensors)"}
+        fa.check_status(dev)
+
+    cpu = None
+    if want_cpu:
+        tflops, heads, secs = oracle_sample(w, args.cpu_seconds, pool, cores, (q, k, v), backward=True)
+        cpu = {"value": tflops, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"{heads} whole heads of the workload (fp64 backward, one head per worker process, "
+                         f"{cores} processes, BLAS single-threaded) in {secs:.1f} s"}
+    if pool is not None:
+        pool.close()
+
+    peaks, src = load_peaks()
+    peak = peaks["bf16_tflops"]
+    achieved = flops / (kernel_ms / 1e3) / 1e12
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "traffic": load_traffic(w.name, "traffic_bwd", BWD_KERNEL_SOURCES),
+            "peak_source": f"bf16 dense burst, {src}",
+            "kernel": f"fa_bwd_prep_kernel<{w.d}> + fa_bwd_tc_kernel<{w.d},0,{str(w.causal).lower()}> + "
+                      f"fa_bwd_tc_kernel<{w.d},1,{str(w.causal).lower()}>",
+            "flops_per_launch": flops,
+            "note": "achieved counts 2.5x the forward's FLOPs over the three kernels' time; the split "
+                    "dK/dV + dQ kernels execute 3.5x (S and dP are recomputed in both)"}
+    if rank == 0:
+        line = {
+            "metric": BWD_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_s / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": dict(config_of(w), **{"pass": "backward", "dO": f"seeded iid normal (seed {w.seed + 1000})"}),
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": 3 * args.steps, "clocks": clocks.summary(),
+            "kernel_ms": {"mean": kernel_ms, "min": min(step_ms), "max": max(step_ms),
+                          "median": statistics.median(step_ms)},
+            "wall_s_timed_region": t_wall,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     from tiled_attention_fwd_gb300.inputs import HEADLINE, WORKLOADS
 
@@ -380,12 +546,16 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU oracle sample budget")
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
+                    help="forward pass (the headline) or backward pass (fa_bwd)")
     args = ap.parse_args(argv)
     if args.impl == "ours":
         args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.pass_ == "bwd":
+        return run_ours_bwd(args, w)
     return run_ours(args, w)
 
 
