@@ -76,6 +76,28 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            int B, int H, int N, int d, float scale, int causal, void* stream);
 
 /*
+ * fa_fwd_strided - fa_fwd with separate query and key lengths and any layout
+ * whose head dimension is contiguous (e.g. [B][N][H][d] as well as
+ * [B][H][N][d]), as the Triton kernel of "FlashAttention-2 from PyTorch to
+ * Triton" takes N_QUERIES, N_KEYS and per-tensor strides.
+ *
+ *   q, o    : bf16, Nq rows per head; element (b, h, i, c) at ptr + b*s[0] + h*s[1] + i*s[2] + c,
+ *             s = q_stride / o_stride.
+ *   k, v    : bf16, Nk rows per head, addressed with k_stride / v_stride likewise.
+ *   *_stride: three element strides {batch, head, row}, each >= 1 and a multiple of 8
+ *             (16 bytes; else FA_ERR_MISALIGNED); read only during the call.
+ *   lse     : fp32, contiguous [B][H][Nq].
+ *   causal  : key k visible to query i iff k <= i (positions from the start of
+ *             both sequences, as in the pages' kernel); keys >= Nk never visible.
+ *   Other arguments, alignment and behaviour as fa_fwd.  o must not overlap q, k, v or itself.
+ */
+int fa_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse,
+                   int B, int H, int Nq, int Nk, int d,
+                   const long long* q_stride, const long long* k_stride,
+                   const long long* v_stride, const long long* o_stride,
+                   float scale, int causal, void* stream);
+
+/*
  * fa_fwd_f32 - fp32 forward pass on the CUDA cores (SIMT), all arithmetic in fp32.
  *
  *   q, k, v, o : device pointers to fp32 [B][H][N][d] (4-byte aligned suffices).

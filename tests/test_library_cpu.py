@@ -102,13 +102,14 @@ def test_missing_library_fails_loudly(tmp_path):
 
 def test_tensor_core_kernels_fit_their_register_split():
     """The d <= 128 kernels launch 512 threads at 128 registers and re-split them
-    (176 x 256 softmax + 72 x 128 correction + 88 x 128 MMA/TMA = 65536); any
+    (176 x 256 softmax + 160 x 128 correction and MMA/TMA, 80/80 or 72/88 = 65536); any
     other launch count would stall setmaxnreg, and none of them may spill."""
     if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
         pytest.skip("nvcc not available")
-    rep = build.ptxas_report({"fa_tc_d32.cu", "fa_tc_d64.cu", "fa_tc_d128.cu", "fa_tc_d256.cu"})
+    files = {f"fa_tc_d{d}{s}.cu" for d in (32, 64, 128, 256) for s in ("", "_strided")}
+    rep = build.ptxas_report(files)
     tc = {k: v for k, v in rep.items() if "fa_fwd_tc_kernel" in k}
-    assert len(tc) == 8
+    assert len(tc) == 16  # 4 head dims x causal / not x contiguous / strided
     for name, r in tc.items():
         assert r["spill_stores"] == 0 and r["spill_loads"] == 0, (name, r)
         if "ILi256E" not in name:
@@ -144,3 +145,14 @@ def test_backward_kernels_do_not_spill():
     assert len(ks) == 15  # per head dimension: 4 tensor-core kernels and 1 preprocessing kernel
     for name, r in ks.items():
         assert r["spill_stores"] == 0 and r["spill_loads"] == 0, (name, r)
+
+
+def test_strided_forward_rejects_bad_arguments_on_host(lib):
+    ok = (1 << 20, 1 << 14, 128)       # {batch, head, row} element strides, multiples of 8
+    bad = (1 << 20, 1 << 14, 132)      # row stride not a multiple of 8 elements
+    args = [FAKE] * 5 + [2, 3, 100, 70, 128]
+    assert fa.fa_fwd_strided(*args, ok, ok, ok, bad, 0.1, 1, None) == -4
+    assert fa.fa_fwd_strided(*args, ok, (0, 8, 8), ok, ok, 0.1, 1, None) == -2
+    assert fa.fa_fwd_strided(*[FAKE] * 5, 2, 3, 100, 0, 128, ok, ok, ok, ok, 0.1, 1, None) == -2
+    assert fa.fa_fwd_strided(*[FAKE] * 5, 2, 3, 100, 70, 48, ok, ok, ok, ok, 0.1, 1, None) == -3
+    assert fa.fa_fwd_strided(*[FAKE] * 4, 0, 2, 3, 100, 70, 128, ok, ok, ok, ok, 0.1, 1, None) == -1

@@ -364,3 +364,26 @@ def test_planted_mistake_fails_a_pin(mutant):
             except Exception as e:  # a crash also counts as caught
                 failures.append(f"{pin.__name__} raised {type(e).__name__}")
     assert failures, f"no pin caught {mutant.__name__}"
+
+
+def test_oracle_with_different_query_and_key_lengths():
+    """Nq != Nk: the pages' kernel takes N_QUERIES and N_KEYS separately and keeps key k for
+    query i iff k < N_KEYS and, when causal, k <= i ("FlashAttention-2 from PyTorch to Triton",
+    the Triton kernel).  torch's SDPA uses the same top-left alignment for non-square causal masks."""
+    rng = np.random.default_rng(17)
+    for nq, nk in ((3, 7), (7, 3), (1, 5), (9, 1), (40, 65)):
+        for d in (2, 8):
+            for causal in (False, True):
+                q = rng.standard_normal((nq, d)) * 2
+                k = rng.standard_normal((nk, d)) * 2
+                v = rng.standard_normal((nk, d))
+                scale = 0.7 / math.sqrt(d)
+                o, lse = oracle.attention_head(q, k, v, scale, causal)
+                tq, tk, tv = (torch.from_numpy(x)[None, None] for x in (q, k, v))
+                o_ref = torch.nn.functional.scaled_dot_product_attention(
+                    tq, tk, tv, is_causal=causal, scale=scale)[0, 0].numpy()
+                s = (q @ k.T) * scale
+                if causal:
+                    s = np.where(np.arange(nk)[None, :] <= np.arange(nq)[:, None], s, -np.inf)
+                assert np.allclose(o, o_ref, atol=1e-12, rtol=0), (nq, nk, d, causal)
+                assert np.allclose(lse, scipy.special.logsumexp(s, axis=1), atol=1e-12, rtol=0), (nq, nk, d, causal)

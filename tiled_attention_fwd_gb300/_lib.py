@@ -22,6 +22,7 @@ _c_size_t = ctypes.c_size_t
 _SIGNATURES = {
     "fa_fwd": (_c_int, [_c_void_p] * 5 + [_c_int] * 4 + [_c_float, _c_int, _c_void_p]),
     "fa_fwd_f32": (_c_int, [_c_void_p] * 5 + [_c_int] * 4 + [_c_float, _c_int, _c_void_p]),
+    "fa_fwd_strided": (_c_int, [_c_void_p] * 5 + [_c_int] * 5 + [_c_void_p] * 4 + [_c_float, _c_int, _c_void_p]),
     "fa_fwd_host_workspace_bytes": (_c_size_t, [_c_int] * 4),
     "fa_fwd_host": (_c_int, [_c_void_p] * 6 + [_c_size_t] + [_c_int] * 4 + [_c_float, _c_int, _c_void_p]),
     "fa_fwd_noalloc": (_c_int, [_c_void_p] * 5 + [_c_int] * 4 + [_c_float, _c_int, _c_void_p]),
@@ -87,6 +88,19 @@ def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream) -> int:
     return load().fa_fwd(q, k, v, o, lse, B, H, N, d, scale, int(bool(causal)), stream)
 
 
+def _strides3(st):
+    arr = (ctypes.c_longlong * 3)(*[int(x) for x in st])
+    return arr
+
+
+def fa_fwd_strided(q, k, v, o, lse, B, H, Nq, Nk, d, q_stride, k_stride, v_stride, o_stride, scale, causal,
+                   stream) -> int:
+    """bf16 forward with Nq != Nk allowed and {batch, head, row} element strides per tensor."""
+    arrs = [_strides3(x) for x in (q_stride, k_stride, v_stride, o_stride)]
+    return load().fa_fwd_strided(q, k, v, o, lse, B, H, Nq, Nk, d, *[ctypes.addressof(a) for a in arrs], scale,
+                                 int(bool(causal)), stream)
+
+
 def fa_fwd_f32(q, k, v, o, lse, B, H, N, d, scale, causal, stream) -> int:
     """fp32 SIMT forward; pointers are integers (device addresses)."""
     return load().fa_fwd_f32(q, k, v, o, lse, B, H, N, d, scale, int(bool(causal)), stream)
@@ -140,33 +154,53 @@ def _stream_handle(torch, device):
 
 
 def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None):
-    """O, L = attention forward of CUDA tensors q, k, v of shape [B, H, N, d].
+    """O, L = attention forward of CUDA tensors q [B, H, Nq, d], k and v [B, H, Nk, d].
 
-    bf16 inputs run the tensor-core kernel (d in {32, 64, 128, 256}); fp32
-    inputs run the SIMT kernel (1 <= d <= 256).  Returns (O, L) with O in the
-    input dtype and L fp32 [B, H, N].  Enqueued on the current stream.
+    bf16 inputs run the tensor-core kernel (d in {32, 64, 128, 256}); any
+    layout whose last dimension is contiguous is accepted (views of [B, N, H, d]
+    storage, for instance), and Nq may differ from Nk (causal: key k visible to
+    query i iff k <= i).  fp32 inputs run the SIMT kernel (contiguous, Nq = Nk,
+    1 <= d <= 256).  Returns (O, L): O like q ([B, H, Nq, d], contiguous unless
+    `out` is given) and L fp32 contiguous [B, H, Nq].  Enqueued on the current stream.
     """
     import torch
 
-    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
-        raise ValueError("q, k, v must share the shape [B, H, N, d]")
+    if q.dim() != 4 or k.dim() != 4 or k.shape != v.shape:
+        raise ValueError("q must be [B, H, Nq, d] and k, v [B, H, Nk, d]")
+    if q.shape[:2] != k.shape[:2] or q.shape[3] != k.shape[3]:
+        raise ValueError("q, k, v must share B, H and d")
     if not (q.is_cuda and k.is_cuda and v.is_cuda):
         raise ValueError("q, k, v must be CUDA tensors")
     if not (q.dtype == k.dtype == v.dtype) or q.dtype not in (torch.bfloat16, torch.float32):
         raise ValueError("q, k, v must all be bf16 or all fp32")
-    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
-        raise ValueError("q, k, v must be contiguous [B, H, N, d]")
-    B, H, N, d = q.shape
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
     if scale is None:
         scale = d ** -0.5
-    o = torch.empty_like(q) if out is None else out
-    l = torch.empty((B, H, N), device=q.device, dtype=torch.float32) if lse is None else lse
+    o = torch.empty(q.shape, device=q.device, dtype=q.dtype) if out is None else out
+    if o.shape != q.shape or o.dtype != q.dtype:
+        raise ValueError("out must have q's shape and dtype")
+    l = torch.empty((B, H, Nq), device=q.device, dtype=torch.float32) if lse is None else lse
+    if l.shape != (B, H, Nq) or l.dtype != torch.float32 or not l.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor [B, H, Nq]")
+    plain = Nq == Nk and all(t.is_contiguous() for t in (q, k, v, o))
     with torch.cuda.device(q.device):
         stream = _stream_handle(torch, q.device)
-        fn = fa_fwd if q.dtype == torch.bfloat16 else fa_fwd_f32
-        rc = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(), B, H, N, d,
-                float(scale), causal, stream)
-    _check(rc, fn.__name__)
+        if plain:
+            fn = fa_fwd if q.dtype == torch.bfloat16 else fa_fwd_f32
+            rc = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(), B, H, Nq, d,
+                    float(scale), causal, stream)
+            name = fn.__name__
+        else:
+            if q.dtype != torch.bfloat16:
+                raise ValueError("fp32 inputs must be contiguous with Nq == Nk")
+            if any(t.stride(3) != 1 for t in (q, k, v, o)):
+                raise ValueError("the last dimension of q, k, v and out must be contiguous")
+            rc = fa_fwd_strided(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(), B, H, Nq, Nk, d,
+                                q.stride()[:3], k.stride()[:3], v.stride()[:3], o.stride()[:3], float(scale), causal,
+                                stream)
+            name = "fa_fwd_strided"
+    _check(rc, name)
     return o, l
 
 

@@ -87,6 +87,33 @@ size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 }  // namespace
 
+// Dispatch of the bf16 forward by head dimension; maps launch failures to FA_ERR_CUDA.
+int launch_tc(const FwdArgs& a, int d, const LaunchCtx& ctx) {
+  long long cq[3], ck[3];
+  contiguous_strides(cq, a.H, a.Nq, d);
+  contiguous_strides(ck, a.H, a.Nk, d);
+  bool contiguous = true;
+  for (int i = 0; i < 3; ++i)
+    contiguous = contiguous && a.qs[i] == cq[i] && a.os[i] == cq[i] && a.ks[i] == ck[i] && a.vs[i] == ck[i];
+  int e = 0;
+  if (contiguous) {
+    switch (d) {
+      case 32: e = launch_tc_d32(a, ctx); break;
+      case 64: e = launch_tc_d64(a, ctx); break;
+      case 128: e = launch_tc_d128(a, ctx); break;
+      default: e = launch_tc_d256(a, ctx); break;
+    }
+  } else {
+    switch (d) {
+      case 32: e = launch_tc_strided_d32(a, ctx); break;
+      case 64: e = launch_tc_strided_d64(a, ctx); break;
+      case 128: e = launch_tc_strided_d128(a, ctx); break;
+      default: e = launch_tc_strided_d256(a, ctx); break;
+    }
+  }
+  return e == 0 ? FA_OK : FA_ERR_CUDA;
+}
+
 int encode_bf16_map(CUtensorMap* map, const void* ptr, int BH, int N, int D, int box_cols, int box_rows,
                     int swizzle_bytes) {
   if (g_encode == nullptr) return -1;
@@ -96,6 +123,22 @@ int encode_bf16_map(CUtensorMap* map, const void* ptr, int BH, int N, int D, int
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUtensorMapSwizzle swz = swizzle_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : -1;
+}
+
+int encode_bf16_map4(CUtensorMap* map, const void* ptr, int B, int H, int N, int D, const long long* stride,
+                     int box_cols, int box_rows, int swizzle_bytes) {
+  if (g_encode == nullptr) return -1;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(stride[2]) * 2, static_cast<cuuint64_t>(stride[1]) * 2,
+                                 static_cast<cuuint64_t>(stride[0]) * 2};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUtensorMapSwizzle swz = swizzle_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box,
                               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? 0 : -1;
@@ -134,17 +177,66 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   fa::DeviceState* s = nullptr;
   rc = fa::current_device_state(&s);
   if (rc != FA_OK) return rc;
-  const fa::LaunchCtx ctx = fa::make_ctx(*s, stream);
-  const int BH = B * H;
-  const bool c = causal != 0;
-  int e = 0;
-  switch (d) {
-    case 32: e = fa::launch_tc_d32(c, q, k, v, o, lse, BH, N, scale, ctx); break;
-    case 64: e = fa::launch_tc_d64(c, q, k, v, o, lse, BH, N, scale, ctx); break;
-    case 128: e = fa::launch_tc_d128(c, q, k, v, o, lse, BH, N, scale, ctx); break;
-    default: e = fa::launch_tc_d256(c, q, k, v, o, lse, BH, N, scale, ctx); break;
+  fa::FwdArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.B = B;
+  a.H = H;
+  a.Nq = N;
+  a.Nk = N;
+  fa::contiguous_strides(a.qs, H, N, d);
+  fa::contiguous_strides(a.ks, H, N, d);
+  fa::contiguous_strides(a.vs, H, N, d);
+  fa::contiguous_strides(a.os, H, N, d);
+  a.scale = scale;
+  a.causal = causal != 0;
+  return fa::launch_tc(a, d, fa::make_ctx(*s, stream));
+}
+
+int fa_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
+                   int d, const long long* q_stride, const long long* k_stride, const long long* v_stride,
+                   const long long* o_stride, float scale, int causal, void* stream) {
+  if (!q || !k || !v || !o || !lse || !q_stride || !k_stride || !v_stride || !o_stride) return FA_ERR_NULL_POINTER;
+  int rc = fa::check_common(B, H, Nq, d, scale);
+  if (rc != FA_OK) return rc;
+  rc = fa::check_common(B, H, Nk, d, scale);
+  if (rc != FA_OK) return rc;
+  if (d != 32 && d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED_D;
+  const long long* all[4] = {q_stride, k_stride, v_stride, o_stride};
+  for (const long long* st : all)
+    for (int i = 0; i < 3; ++i)
+      if (st[i] < 1 || st[i] >= (1LL << 38)) return FA_ERR_BAD_SHAPE;
+  for (const long long* st : all)
+    for (int i = 0; i < 3; ++i)
+      if (st[i] % 8 != 0) return FA_ERR_MISALIGNED;  // 16-byte rows and tiles (TMA, vector stores)
+  if (!fa::aligned16(q) || !fa::aligned16(k) || !fa::aligned16(v) || !fa::aligned16(o) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return FA_ERR_MISALIGNED;
+  fa::DeviceState* s = nullptr;
+  rc = fa::current_device_state(&s);
+  if (rc != FA_OK) return rc;
+  fa::FwdArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.B = B;
+  a.H = H;
+  a.Nq = Nq;
+  a.Nk = Nk;
+  for (int i = 0; i < 3; ++i) {
+    a.qs[i] = q_stride[i];
+    a.ks[i] = k_stride[i];
+    a.vs[i] = v_stride[i];
+    a.os[i] = o_stride[i];
   }
-  return e == 0 ? FA_OK : FA_ERR_CUDA;
+  a.scale = scale;
+  a.causal = causal != 0;
+  return fa::launch_tc(a, d, fa::make_ctx(*s, stream));
 }
 
 int fa_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse, int B, int H, int N, int d,

@@ -47,14 +47,17 @@
 namespace fa {
 
 struct TcParams {
-  int N;                 // sequence length
+  int Nq;                // query rows per head
+  int Nk;                // key / value rows per head
+  int H;                 // heads (unit index bh = b * H + h)
   int BH;                // batch * heads
   int n_kv;              // number of key tiles: ceil(N / BK)
   int n_qb;              // query blocks per head: ceil(N / (BQ * NQT))
   int total_units;       // BH * n_qb
   float scale_log2;      // softmax scale * log2(e)
-  __nv_bfloat16* o;      // [BH][N][D]
-  float* lse;            // [BH][N]
+  __nv_bfloat16* o;      // O(b, h, row, :): contiguous [BH][Nq][D], or (strided kernels)
+  long long o_sb, o_sh, o_sn;  // at o + b * o_sb + h * o_sh + row * o_sn (the d dimension contiguous)
+  float* lse;            // [BH][Nq], contiguous
   int* status;           // device status word
   unsigned long long limit_ns;  // time limit of each device-side wait
 };
@@ -108,13 +111,15 @@ struct TcCfg {
   static constexpr int LOAD_WARP = MMA_WARP + 1;
   static constexpr int THREADS = 32 * (SOFTMAX_WARPS + 8);  // + correction WG + MMA/TMA WG
   // Register split (d <= 128, 512 threads launched at 128 registers each):
-  // softmax 176, correction 72, MMA/TMA warpgroup 88; 2*128*176 + 128*72 + 128*88 = 65536.
+  // softmax 176 and 160 between the correction and the MMA/TMA warpgroups:
+  // 80 / 80, or 72 / 88 where that measured faster (contiguous d = 64; the
+  // strided epilogue needs the correction's 80).  2*128*176 + 128*160 = 65536.
   static constexpr bool SPLIT_REGS = (NQT == 2);
   static constexpr uint32_t REG_SOFTMAX = 176;
-  static constexpr uint32_t REG_CORR = 72;
-  static constexpr uint32_t REG_OTHER = 88;
+  static constexpr uint32_t REG_CORR_OTHER = 160;
+  static constexpr __host__ __device__ uint32_t reg_corr(bool strided) { return (!strided && D == 64) ? 72 : 80; }
   static constexpr int LAUNCH_REGS = 65536 / THREADS > 255 ? 255 : (65536 / THREADS) & ~7;
-  static_assert(!SPLIT_REGS || 2 * 128 * REG_SOFTMAX + 128 * REG_CORR + 128 * REG_OTHER <= THREADS * LAUNCH_REGS,
+  static_assert(!SPLIT_REGS || 2 * 128 * REG_SOFTMAX + 128 * REG_CORR_OTHER <= THREADS * LAUNCH_REGS,
                 "register split exceeds the launch budget");
   static_assert(D == 32 || D == 64 || D == 128 || D == 256, "head dim");
   static_assert(NST >= 2, "K/V stages");
@@ -143,7 +148,7 @@ __device__ __forceinline__ TcUnit tc_decode(int u, const TcParams& p) {
   for (int s = 0; s < 2; ++s) {
     const int r0 = w.row0 + s * C::BQ;
     int n = 0;
-    if (s < C::NQT && r0 < p.N) {
+    if (s < C::NQT && r0 < p.Nq) {
       n = p.n_kv;
       if (CAUSAL) {
         const int last = (r0 + C::BQ - 1) / C::BK + 1;  // tiles holding keys <= last row
@@ -218,7 +223,7 @@ struct TcBars {
 // as soon as the current unit's last S_t product has completed (q_empty(t)).
 //
 // Single-tile mode: per unit, Q, then {K_0, K_1}, then {V_j, K_{j+2}}.
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool STRIDED>
 __device__ __forceinline__ void tc_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                             const TcParams& p, const TcBars<D>& bar, uint32_t base,
                                             const WaitGuard& g) {
@@ -230,8 +235,15 @@ __device__ __forceinline__ void tc_producer(const CUtensorMap* tm_q, const CUten
   uint32_t last_par = 0;  // bit i: parity of stage i's latest load
   int last_q[2] = {-1, -1};  // per Q tile: index (within this CTA) of the latest unit whose tile was loaded
   bool ok = true;
+  // Tile j (rows j*BK ..) of unit bh.  Strided tensors are 4-D maps {d, N, H, B}
+  // (coordinates h, b), contiguous ones 3-D maps {d, N, B*H} (coordinate bh).
   auto load_tile = [&](const CUtensorMap* tm, uint32_t dst, uint32_t full, int j, int bh) {
-    for (int r = 0; r < C::NR; ++r) tma_load_3d(dst + r * C::KV_REGION, tm, full, r * C::RC, j * C::BK, bh, pol_kv);
+    for (int r = 0; r < C::NR; ++r) {
+      if constexpr (STRIDED)
+        tma_load_4d(dst + r * C::KV_REGION, tm, full, r * C::RC, j * C::BK, bh % p.H, bh / p.H, pol_kv);
+      else
+        tma_load_3d(dst + r * C::KV_REGION, tm, full, r * C::RC, j * C::BK, bh, pol_kv);
+    }
   };
   // Q tiles of unit x, the qi-th unit of this CTA.
   auto load_q = [&](const TcUnit& x, int qi) -> bool {
@@ -239,8 +251,12 @@ __device__ __forceinline__ void tc_producer(const CUtensorMap* tm_q, const CUten
       if (!wait_bar(bar.q_empty(t), (qi & 1) ^ 1, g, kStatusTimeoutLoad)) return false;
       mbar_arrive_expect_tx(bar.q_full(t), C::Q_TILE);
       for (int r = 0; r < C::NR; ++r)
-        tma_load_3d(base + C::OFF_Q + t * C::Q_TILE + r * C::Q_REGION, tm_q, bar.q_full(t), r * C::RC,
-                    x.row0 + t * C::BQ, x.bh, pol_q);
+        if constexpr (STRIDED)
+          tma_load_4d(base + C::OFF_Q + t * C::Q_TILE + r * C::Q_REGION, tm_q, bar.q_full(t), r * C::RC,
+                      x.row0 + t * C::BQ, x.bh % p.H, x.bh / p.H, pol_q);
+        else
+          tma_load_3d(base + C::OFF_Q + t * C::Q_TILE + r * C::Q_REGION, tm_q, bar.q_full(t), r * C::RC,
+                      x.row0 + t * C::BQ, x.bh, pol_q);
       last_q[t] = qi;
     }
     return true;
@@ -562,12 +578,12 @@ __device__ __forceinline__ void tc_softmax(const TcParams& p, const TcBars<D>& b
           for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(raw_s[c][i]);
       }
       const int key0 = j * C::BK;
-      const bool need_mask = (CAUSAL && key0 + C::BK - 1 > row0) || (key0 + C::BK > p.N);
+      const bool need_mask = (CAUSAL && key0 + C::BK - 1 > row0) || (key0 + C::BK > p.Nk);
       if (need_mask) {
 #pragma unroll
         for (int c = 0; c < C::BK; ++c) {
           const int key = key0 + c;
-          if (key >= p.N || (CAUSAL && key > row)) s[c] = -INFINITY;
+          if (key >= p.Nk || (CAUSAL && key > row)) s[c] = -INFINITY;
         }
       }
       // Row max: 8 chains of three-input maxima over interleaved columns.
@@ -627,7 +643,7 @@ __device__ __forceinline__ void tc_softmax(const TcParams& p, const TcBars<D>& b
 }
 
 // ------------------------------------------------------------------ correction + epilogue
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool STRIDED>
 __device__ __forceinline__ void tc_correction(const TcParams& p, const TcBars<D>& bar, uint8_t* gbase, uint32_t tmem,
                                               int quarter, int lane, const WaitGuard& g) {
   using C = TcCfg<D>;
@@ -700,7 +716,11 @@ __device__ __forceinline__ void tc_correction(const TcParams& p, const TcBars<D>
     const uint64_t il2 = f2_pack(inv_l, inv_l);
     const int row = w.row0 + t * C::BQ + r;
     const uint32_t to = tmem + lane_off + C::TM_O + t * D;
-    __nv_bfloat16* orow = p.o + (static_cast<size_t>(w.bh) * p.N + row) * D;
+    __nv_bfloat16* orow;
+    if constexpr (STRIDED)
+      orow = p.o + (w.bh / p.H) * p.o_sb + (w.bh % p.H) * p.o_sh + static_cast<long long>(row) * p.o_sn;
+    else
+      orow = p.o + (static_cast<size_t>(w.bh) * p.Nq + row) * D;
 #pragma unroll 1
     for (int c = 0; c < D / 32; ++c) {
       uint32_t v[32];
@@ -712,14 +732,14 @@ __device__ __forceinline__ void tc_correction(const TcParams& p, const TcBars<D>
         const float2 y = f2_unpack(f2_mul(f2_pack(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), il2));
         packed[i] = pack_bf16x2(y.x, y.y);
       }
-      if (row < p.N) {
+      if (row < p.Nq) {
         uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
           dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
       }
     }
-    if (row < p.N) p.lse[static_cast<size_t>(w.bh) * p.N + row] = (mrow + log2f(lrow)) * 0.69314718055994531f;
+    if (row < p.Nq) p.lse[static_cast<size_t>(w.bh) * p.Nq + row] = (mrow + log2f(lrow)) * 0.69314718055994531f;
     tc_fence_before();
     release_o(t);  // O may be overwritten by the next unit's first P V
     return true;
@@ -741,7 +761,7 @@ __device__ __forceinline__ void tc_correction(const TcParams& p, const TcBars<D>
 }
 
 // ------------------------------------------------------------------ kernel
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool STRIDED>
 __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
     fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
@@ -798,11 +818,11 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
     if constexpr (C::SPLIT_REGS) regs_increase<C::REG_SOFTMAX>();
     tc_softmax<D, CAUSAL>(p, bar, gbase, tmem, warp >> 2, warp & 3, lane, g);
   } else if (warp < C::SOFTMAX_WARPS + 4) {
-    if constexpr (C::SPLIT_REGS) regs_decrease<C::REG_CORR>();
-    tc_correction<D, CAUSAL>(p, bar, gbase, tmem, warp & 3, lane, g);
+    if constexpr (C::SPLIT_REGS) regs_decrease<C::reg_corr(STRIDED)>();
+    tc_correction<D, CAUSAL, STRIDED>(p, bar, gbase, tmem, warp & 3, lane, g);
   } else {
-    if constexpr (C::SPLIT_REGS) regs_decrease<C::REG_OTHER>();
-    if (warp == C::LOAD_WARP && lane == 0) tc_producer<D, CAUSAL>(&tm_q, &tm_k, &tm_v, p, bar, base, g);
+    if constexpr (C::SPLIT_REGS) regs_decrease<C::REG_CORR_OTHER - C::reg_corr(STRIDED)>();
+    if (warp == C::LOAD_WARP && lane == 0) tc_producer<D, CAUSAL, STRIDED>(&tm_q, &tm_k, &tm_v, p, bar, base, g);
     if (warp == C::MMA_WARP) tc_mma<D, CAUSAL>(p, bar, base, tmem, g);
   }
 

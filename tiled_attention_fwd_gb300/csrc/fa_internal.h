@@ -18,6 +18,42 @@ struct LaunchCtx {
   cudaStream_t stream;
 };
 
+// Arguments of the bf16 forward pass.  Each of q, k, v, o is addressed as
+// ptr + b * stride[0] + h * stride[1] + row * stride[2] + c (elements; the d
+// dimension is contiguous); q and o have Nq rows per head, k and v Nk.  lse
+// is contiguous [B][H][Nq].
+struct FwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  int B;
+  int H;
+  int Nq;
+  int Nk;
+  long long qs[3];
+  long long ks[3];
+  long long vs[3];
+  long long os[3];
+  float scale;
+  bool causal;
+};
+
+// Contiguous [B][H][N][d] strides.
+inline void contiguous_strides(long long* st, int H, int N, int d) {
+  st[2] = d;
+  st[1] = static_cast<long long>(N) * d;
+  st[0] = static_cast<long long>(H) * N * d;
+}
+
+// Encode a 4-D TMA descriptor over a bf16 tensor addressed as above:
+// dimensions {D, N, H, B}, byte strides from `stride` (elements: batch, head,
+// row), box {box_cols, box_rows, 1, 1}, swizzle span `swizzle_bytes` (64 or
+// 128).  Returns 0 on success.
+int encode_bf16_map4(CUtensorMap* map, const void* ptr, int B, int H, int N, int D, const long long* stride,
+                     int box_cols, int box_rows, int swizzle_bytes);
+
 // Encode a 3-D TMA descriptor over a contiguous bf16 [BH][N][D] tensor:
 // dimensions {D, N, BH}, box {box_cols, box_rows, 1}, swizzle span
 // `swizzle_bytes` (64 or 128).  Returns 0 on success.
@@ -32,14 +68,15 @@ unsigned long long wait_limit_ns();
 
 // bf16 tensor-core forward for one head dimension; returns a cudaError_t-like
 // code (0 = launched).  Defined in fa_tc_d<D>.cu.
-int launch_tc_d32(bool causal, const void* q, const void* k, const void* v, void* o, float* lse, int BH, int N,
-                  float scale, const LaunchCtx& ctx);
-int launch_tc_d64(bool causal, const void* q, const void* k, const void* v, void* o, float* lse, int BH, int N,
-                  float scale, const LaunchCtx& ctx);
-int launch_tc_d128(bool causal, const void* q, const void* k, const void* v, void* o, float* lse, int BH, int N,
-                   float scale, const LaunchCtx& ctx);
-int launch_tc_d256(bool causal, const void* q, const void* k, const void* v, void* o, float* lse, int BH, int N,
-                   float scale, const LaunchCtx& ctx);
+int launch_tc_d32(const FwdArgs& a, const LaunchCtx& ctx);
+int launch_tc_d64(const FwdArgs& a, const LaunchCtx& ctx);
+int launch_tc_d128(const FwdArgs& a, const LaunchCtx& ctx);
+int launch_tc_d256(const FwdArgs& a, const LaunchCtx& ctx);
+// The same for strided tensors (4-D tensor maps).  Defined in fa_tc_d<D>_strided.cu.
+int launch_tc_strided_d32(const FwdArgs& a, const LaunchCtx& ctx);
+int launch_tc_strided_d64(const FwdArgs& a, const LaunchCtx& ctx);
+int launch_tc_strided_d128(const FwdArgs& a, const LaunchCtx& ctx);
+int launch_tc_strided_d256(const FwdArgs& a, const LaunchCtx& ctx);
 
 // Arguments of the backward pass (device pointers; bf16 tensors [BH][N][d],
 // lse fp32 [BH][N]; l2 and dsum are workspace vectors [BH][n_pad]).
@@ -67,6 +104,11 @@ struct BwdArgs {
 int launch_bwd_d32(const BwdArgs& a, const LaunchCtx& ctx);
 int launch_bwd_d64(const BwdArgs& a, const LaunchCtx& ctx);
 int launch_bwd_d128(const BwdArgs& a, const LaunchCtx& ctx);
+
+// The bf16 forward for d in {32, 64, 128, 256}; takes the contiguous kernels
+// when every tensor is contiguous [B][H][N][d], else the strided ones; returns
+// an FA_* code.  Defined in fa_api.cu.
+int launch_tc(const FwdArgs& a, int d, const LaunchCtx& ctx);
 
 // fp32 SIMT forward, 1 <= d <= 256.  Defined in fa_simt.cu.
 int launch_simt(bool causal, const float* q, const float* k, const float* v, float* o, float* lse, int BH, int N,

@@ -87,14 +87,21 @@ extern "C" int fa_fwd_noalloc(const void* q, const void* k, const void* v, void*
   ctx.limit_ns = fa::wait_limit_ns();
   ctx.num_sms = s->num_sms;
   ctx.stream = st;
-  const int BH = B * H;
-  const bool c = causal != 0;
-  int e = 0;
-  switch (d) {
-    case 32: e = fa::launch_tc_d32(c, q, k, v, o, lse, BH, N, scale, ctx); break;
-    case 64: e = fa::launch_tc_d64(c, q, k, v, o, lse, BH, N, scale, ctx); break;
-    case 128: e = fa::launch_tc_d128(c, q, k, v, o, lse, BH, N, scale, ctx); break;
-    default: e = fa::launch_tc_d256(c, q, k, v, o, lse, BH, N, scale, ctx); break;
-  }
-  return e == 0 ? FA_OK : FA_ERR_CUDA;
+  fa::FwdArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.B = B;
+  a.H = H;
+  a.Nq = N;
+  a.Nk = N;
+  fa::contiguous_strides(a.qs, H, N, d);
+  fa::contiguous_strides(a.ks, H, N, d);
+  fa::contiguous_strides(a.vs, H, N, d);
+  fa::contiguous_strides(a.os, H, N, d);
+  a.scale = scale;
+  a.causal = causal != 0;
+  return fa::launch_tc(a, d, ctx);
 }

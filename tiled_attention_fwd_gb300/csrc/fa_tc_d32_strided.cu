@@ -1,0 +1,4 @@
+// Tensor-core forward pass on strided tensors (4-D tensor maps), head dimension 32, causal and non-causal.
+#include "fa_tc_launch.cuh"
+
+FA_DEFINE_TC_STRIDED_LAUNCHER(32)

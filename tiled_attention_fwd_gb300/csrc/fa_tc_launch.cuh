@@ -9,11 +9,10 @@
 
 namespace fa {
 
-template <int D, bool CAUSAL>
-int launch_tc_impl(const void* q, const void* k, const void* v, void* o, float* lse, int BH, int N, float scale,
-                   const LaunchCtx& ctx) {
+template <int D, bool CAUSAL, bool STRIDED>
+int launch_tc_impl(const FwdArgs& a, const LaunchCtx& ctx) {
   using C = TcCfg<D>;
-  auto kernel = fa_fwd_tc_kernel<D, CAUSAL>;
+  auto kernel = fa_fwd_tc_kernel<D, CAUSAL, STRIDED>;
   if constexpr (C::SPLIT_REGS) {
     // The warpgroups re-split the registers the block was launched with
     // (setmaxnreg); the split is sized for exactly LAUNCH_REGS per thread.  A
@@ -32,18 +31,29 @@ int launch_tc_impl(const void* q, const void* k, const void* v, void* o, float* 
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
   if (e != cudaSuccess) return static_cast<int>(e);
   CUtensorMap mq, mk, mv;
-  if (encode_bf16_map(&mq, q, BH, N, D, C::RC, C::BQ, C::SWB) != 0) return -1;
-  if (encode_bf16_map(&mk, k, BH, N, D, C::RC, C::BK, C::SWB) != 0) return -1;
-  if (encode_bf16_map(&mv, v, BH, N, D, C::RC, C::BK, C::SWB) != 0) return -1;
+  if constexpr (STRIDED) {
+    if (encode_bf16_map4(&mq, a.q, a.B, a.H, a.Nq, D, a.qs, C::RC, C::BQ, C::SWB) != 0) return -1;
+    if (encode_bf16_map4(&mk, a.k, a.B, a.H, a.Nk, D, a.ks, C::RC, C::BK, C::SWB) != 0) return -1;
+    if (encode_bf16_map4(&mv, a.v, a.B, a.H, a.Nk, D, a.vs, C::RC, C::BK, C::SWB) != 0) return -1;
+  } else {
+    if (encode_bf16_map(&mq, a.q, a.B * a.H, a.Nq, D, C::RC, C::BQ, C::SWB) != 0) return -1;
+    if (encode_bf16_map(&mk, a.k, a.B * a.H, a.Nk, D, C::RC, C::BK, C::SWB) != 0) return -1;
+    if (encode_bf16_map(&mv, a.v, a.B * a.H, a.Nk, D, C::RC, C::BK, C::SWB) != 0) return -1;
+  }
   TcParams p;
-  p.N = N;
-  p.BH = BH;
-  p.n_kv = (N + C::BK - 1) / C::BK;
-  p.n_qb = (N + C::BQ * C::NQT - 1) / (C::BQ * C::NQT);
-  p.total_units = BH * p.n_qb;
-  p.scale_log2 = scale * 1.4426950408889634f;
-  p.o = static_cast<__nv_bfloat16*>(o);
-  p.lse = lse;
+  p.Nq = a.Nq;
+  p.Nk = a.Nk;
+  p.H = a.H;
+  p.BH = a.B * a.H;
+  p.n_kv = (a.Nk + C::BK - 1) / C::BK;
+  p.n_qb = (a.Nq + C::BQ * C::NQT - 1) / (C::BQ * C::NQT);
+  p.total_units = p.BH * p.n_qb;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.o = static_cast<__nv_bfloat16*>(a.o);
+  p.o_sb = a.os[0];
+  p.o_sh = a.os[1];
+  p.o_sn = a.os[2];
+  p.lse = a.lse;
   p.status = ctx.status;
   p.limit_ns = ctx.limit_ns;
   const int grid = p.total_units < ctx.num_sms ? p.total_units : ctx.num_sms;
@@ -53,11 +63,18 @@ int launch_tc_impl(const void* q, const void* k, const void* v, void* o, float* 
 
 }  // namespace fa
 
-#define FA_DEFINE_TC_LAUNCHER(DIM)                                                                         \
-  namespace fa {                                                                                           \
-  int launch_tc_d##DIM(bool causal, const void* q, const void* k, const void* v, void* o, float* lse, int BH, \
-                       int N, float scale, const LaunchCtx& ctx) {                                         \
-    return causal ? launch_tc_impl<DIM, true>(q, k, v, o, lse, BH, N, scale, ctx)                          \
-                  : launch_tc_impl<DIM, false>(q, k, v, o, lse, BH, N, scale, ctx);                        \
-  }                                                                                                        \
+// Contiguous [B][H][N][d] tensors (3-D maps, the fast path), in fa_tc_d<D>.cu.
+#define FA_DEFINE_TC_LAUNCHER(DIM)                                                                     \
+  namespace fa {                                                                                       \
+  int launch_tc_d##DIM(const FwdArgs& a, const LaunchCtx& ctx) {                                       \
+    return a.causal ? launch_tc_impl<DIM, true, false>(a, ctx) : launch_tc_impl<DIM, false, false>(a, ctx); \
+  }                                                                                                    \
+  }
+
+// Any strides with a contiguous d dimension (4-D maps), in fa_tc_d<D>_strided.cu.
+#define FA_DEFINE_TC_STRIDED_LAUNCHER(DIM)                                                           \
+  namespace fa {                                                                                     \
+  int launch_tc_strided_d##DIM(const FwdArgs& a, const LaunchCtx& ctx) {                             \
+    return a.causal ? launch_tc_impl<DIM, true, true>(a, ctx) : launch_tc_impl<DIM, false, true>(a, ctx); \
+  }                                                                                                  \
   }
