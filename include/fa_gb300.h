@@ -116,11 +116,15 @@ int fa_fwd_f32(const float* q, const float* k, const float* v, float* o, float* 
 size_t fa_fwd_host_workspace_bytes(int B, int H, int N, int d);
 
 /*
- * fa_fwd_host - fa_fwd on HOST buffers: enqueues on `stream` the host-to-device
- * copies of q, k, v into `workspace`, the forward pass, and the device-to-host
- * copies of O and L into o and lse.  Host buffers should be page-locked for
- * the copies to be asynchronous.  The caller synchronises `stream` before
- * reading o and lse or reusing the inputs.
+ * fa_fwd_host - fa_fwd on HOST buffers: the host-to-device copies of q, k, v
+ * into `workspace`, the forward pass, and the device-to-host copies of O and
+ * L into o and lse, pipelined over up to 8 chunks of heads so that copies in,
+ * kernels and copies out overlap.  The copies run on two internal streams of
+ * the library that start after the work already enqueued on `stream`, and
+ * `stream` waits for them at the end: the call is ordered on `stream` like a
+ * single kernel (also under stream capture).  Host buffers should be
+ * page-locked for the copies to be asynchronous.  The caller synchronises
+ * `stream` before reading o and lse or reusing the inputs.
  *
  *   q, k, v   : host pointers to bf16 [B][H][N][d].
  *   o, lse    : host pointers receiving bf16 O and fp32 L.

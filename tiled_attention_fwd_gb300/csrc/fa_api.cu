@@ -16,12 +16,27 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
+constexpr int kHostChunks = 8;  // fa_fwd_host pipelines its copies and kernels over this many head chunks
+
+// Streams and events of fa_fwd_host's copy/compute pipeline, created on first use.
+struct HostPipeline {
+  bool ready = false;
+  std::mutex mutex;  // one enqueue sequence at a time (the events are reused)
+  cudaStream_t s_in = nullptr;
+  cudaStream_t s_out = nullptr;
+  cudaEvent_t fork = nullptr;
+  cudaEvent_t join = nullptr;
+  cudaEvent_t in[kHostChunks] = {};
+  cudaEvent_t done[kHostChunks] = {};
+};
+
 struct DeviceState {
   bool ready = false;
   int* status = nullptr;  // one device int, zeroed at creation
   int num_sms = 0;
   int cc_major = 0;
   int cc_minor = 0;
+  HostPipeline pipe;
 };
 
 std::mutex g_mutex;
@@ -84,6 +99,26 @@ LaunchCtx make_ctx(const DeviceState& s, void* stream) {
 }
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Create fa_fwd_host's streams and events for device state `s` (once).
+int host_pipeline(DeviceState* s, HostPipeline** out) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  HostPipeline& hp = s->pipe;
+  if (!hp.ready) {
+    if (cudaStreamCreateWithFlags(&hp.s_in, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&hp.s_out, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&hp.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&hp.join, cudaEventDisableTiming) != cudaSuccess)
+      return FA_ERR_CUDA;
+    for (int i = 0; i < kHostChunks; ++i)
+      if (cudaEventCreateWithFlags(&hp.in[i], cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&hp.done[i], cudaEventDisableTiming) != cudaSuccess)
+        return FA_ERR_CUDA;
+    hp.ready = true;
+  }
+  *out = &hp;
+  return FA_OK;
+}
 
 }  // namespace
 
@@ -274,21 +309,53 @@ int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA_ERR_MISALIGNED;
   const size_t need = fa_fwd_host_workspace_bytes(B, H, N, d);
   if (workspace_bytes < need) return FA_ERR_WORKSPACE;
-  const size_t tbytes = static_cast<size_t>(B) * H * N * d * 2;
-  const size_t lbytes = static_cast<size_t>(B) * H * N * 4;
-  const size_t step = fa::round256(tbytes);
-  char* w = static_cast<char*>(workspace);
-  void *dq = w, *dk = w + step, *dv = w + 2 * step, *dout = w + 3 * step;
-  float* dl = reinterpret_cast<float*>(w + 4 * step);
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (cudaMemcpyAsync(dq, q, tbytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
-      cudaMemcpyAsync(dk, k, tbytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
-      cudaMemcpyAsync(dv, v, tbytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
-    return FA_ERR_CUDA;
-  rc = fa_fwd(dq, dk, dv, dout, dl, B, H, N, d, scale, causal, stream);
+  fa::DeviceState* s = nullptr;
+  rc = fa::current_device_state(&s);
   if (rc != FA_OK) return rc;
-  if (cudaMemcpyAsync(o, dout, tbytes, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
-      cudaMemcpyAsync(lse, dl, lbytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+  fa::HostPipeline* hp = nullptr;
+  rc = fa::host_pipeline(s, &hp);
+  if (rc != FA_OK) return rc;
+  const size_t per_head = static_cast<size_t>(N) * d * 2;  // bytes of one head of Q, K, V or O
+  const size_t step = fa::round256(static_cast<size_t>(B) * H * per_head);
+  char* w = static_cast<char*>(workspace);
+  char *dq = w, *dk = w + step, *dv = w + 2 * step, *dout = w + 3 * step;
+  float* dl = reinterpret_cast<float*>(w + 4 * step);
+  const char* hq = static_cast<const char*>(q);
+  const char* hk = static_cast<const char*>(k);
+  const char* hv = static_cast<const char*>(v);
+  char* ho = static_cast<char*>(o);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // Pipeline over chunks of heads: the copy-in stream brings chunk c's Q, K, V
+  // while `stream` runs the kernel of chunk c - 1 and the copy-out stream
+  // returns chunk c - 2's O and L.  Both copy streams fork from `stream` and
+  // `stream` joins the copy-out stream at the end, so the call is ordered on
+  // `stream` like a single kernel.
+  const int BH = B * H;
+  const int nch = BH < fa::kHostChunks ? BH : fa::kHostChunks;
+  std::lock_guard<std::mutex> lock(hp->mutex);
+  if (cudaEventRecord(hp->fork, st) != cudaSuccess || cudaStreamWaitEvent(hp->s_in, hp->fork, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(hp->s_out, hp->fork, 0) != cudaSuccess)
+    return FA_ERR_CUDA;
+  for (int c = 0; c < nch; ++c) {
+    const int h0 = static_cast<int>(static_cast<long long>(BH) * c / nch);
+    const int h1 = static_cast<int>(static_cast<long long>(BH) * (c + 1) / nch);
+    const size_t off = static_cast<size_t>(h0) * per_head, bytes = static_cast<size_t>(h1 - h0) * per_head;
+    if (cudaMemcpyAsync(dq + off, hq + off, bytes, cudaMemcpyHostToDevice, hp->s_in) != cudaSuccess ||
+        cudaMemcpyAsync(dk + off, hk + off, bytes, cudaMemcpyHostToDevice, hp->s_in) != cudaSuccess ||
+        cudaMemcpyAsync(dv + off, hv + off, bytes, cudaMemcpyHostToDevice, hp->s_in) != cudaSuccess ||
+        cudaEventRecord(hp->in[c], hp->s_in) != cudaSuccess || cudaStreamWaitEvent(st, hp->in[c], 0) != cudaSuccess)
+      return FA_ERR_CUDA;
+    rc = fa_fwd(dq + off, dk + off, dv + off, dout + off, dl + static_cast<size_t>(h0) * N, 1, h1 - h0, N, d, scale,
+                causal, stream);
+    if (rc != FA_OK) return rc;
+    const size_t lrows = static_cast<size_t>(h1 - h0) * N;
+    if (cudaEventRecord(hp->done[c], st) != cudaSuccess || cudaStreamWaitEvent(hp->s_out, hp->done[c], 0) != cudaSuccess ||
+        cudaMemcpyAsync(ho + off, dout + off, bytes, cudaMemcpyDeviceToHost, hp->s_out) != cudaSuccess ||
+        cudaMemcpyAsync(lse + static_cast<size_t>(h0) * N, dl + static_cast<size_t>(h0) * N, lrows * 4,
+                        cudaMemcpyDeviceToHost, hp->s_out) != cudaSuccess)
+      return FA_ERR_CUDA;
+  }
+  if (cudaEventRecord(hp->join, hp->s_out) != cudaSuccess || cudaStreamWaitEvent(st, hp->join, 0) != cudaSuccess)
     return FA_ERR_CUDA;
   return FA_OK;
 }
