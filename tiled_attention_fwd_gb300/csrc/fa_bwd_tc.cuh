@@ -38,7 +38,7 @@ struct BwdParams {
   int BH;                // batch * heads
   int n_pad;             // row stride of the l2 / dsum vectors: N rounded up to 64
   int n_m;               // 128-row tiles of the fixed operands per head: ceil(N / 128)
-  int n_s;               // 64-row streamed tiles per head: ceil(N / 64)
+  int n_s;               // streamed tiles per head: ceil(N / BS)
   int total_units;       // BH * n_m
   float scale;           // softmax scale (dK and dQ carry one factor of it)
   float scale_log2;      // scale * log2(e)
@@ -54,7 +54,10 @@ template <int D, int MODE>
 struct BwdCfg {
   static constexpr bool KV = (MODE == 0);
   static constexpr int BM = 128;                         // fixed-tile rows = TMEM lanes
-  static constexpr int BS = 64;                          // streamed-tile rows
+  // Streamed-tile rows: 64 in MODE 0, where TMEM holds two accumulators
+  // (4 * 64 + 2 * D columns at d = 128); 96 in MODE 1, where it holds one
+  // (4 * 96 + D): fewer, larger S and dP products per FLOP for the MMA warp.
+  static constexpr int BS = KV ? 64 : 96;
   static constexpr int SWB = (D * 2 >= 128) ? 128 : D * 2;  // swizzle span in bytes
   static constexpr uint32_t SWZ = (SWB == 128) ? 2u : 4u;   // descriptor swizzle code
   static constexpr int RC = SWB / 2;                     // bf16 columns per swizzle region
@@ -114,11 +117,11 @@ __device__ __forceinline__ BwdUnit bwd_decode(int u, const BwdParams& p) {
   w.bh = u % p.BH;
   w.m0 = mt * 128;
   if (MODE == 0) {
-    w.s_begin = CAUSAL ? w.m0 / 64 : 0;  // query tiles holding some query >= the first key
+    w.s_begin = CAUSAL ? w.m0 / BwdCfg<D, MODE>::BS : 0;  // query tiles holding some query >= the first key
     w.s_end = p.n_s;
   } else {
     w.s_begin = 0;
-    const int last = (w.m0 + 127) / 64 + 1;  // key tiles holding some key <= the last query
+    const int last = (w.m0 + 127) / BwdCfg<D, MODE>::BS + 1;  // key tiles holding some key <= the last query
     w.s_end = (CAUSAL && last < p.n_s) ? last : p.n_s;
   }
   return w;
@@ -165,7 +168,7 @@ __device__ __forceinline__ bool bwd_wait_drain(uint32_t bar, uint32_t parity, co
 
 // ------------------------------------------------------------------ TMA producer
 // One thread.  Per unit: the two fixed tiles (A1, A2: 128 rows each), then one
-// stage per streamed tile: B1 and B2 (64 rows each) and, in MODE 0, the 64
+// stage per streamed tile: B1 and B2 (BS rows each) and, in MODE 0, the 64
 // streamed rows' L * log2(e) and D.
 //   MODE 0: A1 = K, A2 = V, B1 = Q, B2 = dO.   MODE 1: A1 = Q, A2 = dO, B1 = K, B2 = V.
 template <int D, int MODE, bool CAUSAL>
