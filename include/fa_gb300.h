@@ -137,7 +137,7 @@ int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse
 
 /*
  * fa_bwd_workspace_bytes - size of the device workspace fa_bwd needs: two fp32
- * vectors of B*H*round_up(N, 64) rows (L * log2(e) and D = rowsum(dO * O)),
+ * vectors of B*H*round_up(N, 192) rows (L * log2(e) and D = rowsum(dO * O)),
  * each 256-byte aligned.  Returns 0 for invalid shapes.
  */
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);

@@ -121,7 +121,7 @@ def test_tensor_core_kernels_fit_their_register_split():
 def test_backward_workspace_size_and_host_checks(lib):
     r256 = lambda x: (x + 255) // 256 * 256
     n = fa.fa_bwd_workspace_bytes(2, 3, 100, 64)
-    assert n == 2 * r256(2 * 3 * 128 * 4)  # N padded to a multiple of 64
+    assert n == 2 * r256(2 * 3 * 192 * 4)  # N padded to a multiple of 192
     assert fa.fa_bwd_workspace_bytes(2, 3, 0, 64) == 0
     ws = FAKE * 16
     common = (2, 3, 100, 64, 0.125, 0)

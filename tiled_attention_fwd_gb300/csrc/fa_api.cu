@@ -362,7 +362,7 @@ int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse
 
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
   if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
-  const size_t n_pad = (static_cast<size_t>(N) + 63) / 64 * 64;
+  const size_t n_pad = (static_cast<size_t>(N) + 191) / 192 * 192;  // a multiple of both streamed-tile heights
   return 2 * fa::round256(static_cast<size_t>(B) * H * n_pad * 4);
 }
 
@@ -394,7 +394,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
   a.dv = dv;
   a.BH = B * H;
   a.N = N;
-  a.n_pad = (N + 63) / 64 * 64;
+  a.n_pad = (N + 191) / 192 * 192;
   a.scale = scale;
   a.causal = causal != 0;
   a.l2 = static_cast<float*>(workspace);

@@ -36,7 +36,7 @@ namespace fa {
 struct BwdParams {
   int N;                 // sequence length
   int BH;                // batch * heads
-  int n_pad;             // row stride of the l2 / dsum vectors: N rounded up to 64
+  int n_pad;             // row stride of the l2 / dsum vectors: N rounded up to 192 (a multiple of every BS)
   int n_m;               // 128-row tiles of the fixed operands per head: ceil(N / 128)
   int n_s;               // streamed tiles per head: ceil(N / BS)
   int total_units;       // BH * n_m
@@ -54,10 +54,11 @@ template <int D, int MODE>
 struct BwdCfg {
   static constexpr bool KV = (MODE == 0);
   static constexpr int BM = 128;                         // fixed-tile rows = TMEM lanes
-  // Streamed-tile rows: 64 in MODE 0, where TMEM holds two accumulators
-  // (4 * 64 + 2 * D columns at d = 128); 96 in MODE 1, where it holds one
-  // (4 * 96 + D): fewer, larger S and dP products per FLOP for the MMA warp.
-  static constexpr int BS = KV ? 64 : 96;
+  // Streamed-tile rows: 96 where TMEM holds the double-buffered S and dP and
+  // the accumulators (4 * 96 + D in MODE 1; 4 * 96 + 2 * D in MODE 0 for
+  // d <= 64), else 64 (MODE 0 at d = 128: 4 * 64 + 2 * 128 = 512 columns).
+  // Larger tiles mean fewer, larger S and dP products per FLOP for the MMA warp.
+  static constexpr int BS = (KV && D == 128) ? 64 : 96;
   static constexpr int SWB = (D * 2 >= 128) ? 128 : D * 2;  // swizzle span in bytes
   static constexpr uint32_t SWZ = (SWB == 128) ? 2u : 4u;   // descriptor swizzle code
   static constexpr int RC = SWB / 2;                     // bf16 columns per swizzle region
@@ -205,7 +206,7 @@ __device__ __forceinline__ void bwd_producer(const CUtensorMap* tm_a1, const CUt
         tma_load_3d(s0 + C::S_TILE + r * C::S_REGION, tm_b2, full, r * C::RC, s * C::BS, w.bh, pol_str);
       }
       if constexpr (C::KV) {
-        // s * 64 + 64 <= n_pad, and n_pad is a multiple of 64: 256-byte aligned, in bounds.
+        // s * BS + BS <= n_pad (a multiple of BS), and BS * 4 is a multiple of 16: aligned, in bounds.
         const size_t off = static_cast<size_t>(w.bh) * p.n_pad + static_cast<size_t>(s) * C::BS;
         bulk_load(s0 + 2 * C::S_TILE, p.l2 + off, C::VEC_BYTES, full);
         bulk_load(s0 + 2 * C::S_TILE + C::VEC_BYTES, p.dsum + off, C::VEC_BYTES, full);

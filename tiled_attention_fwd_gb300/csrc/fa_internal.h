@@ -92,7 +92,7 @@ struct BwdArgs {
   void* dv;
   int BH;
   int N;
-  int n_pad;       // N rounded up to a multiple of 64
+  int n_pad;       // N rounded up to a multiple of 192
   float scale;
   bool causal;
   float* l2;
