@@ -138,7 +138,8 @@ int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse
 /*
  * fa_bwd_workspace_bytes - size of the device workspace fa_bwd needs: two fp32
  * vectors of B*H*round_up(N, 192) rows (L * log2(e) and D = rowsum(dO * O)),
- * each 256-byte aligned.  Returns 0 for invalid shapes.
+ * each 256-byte aligned.  For fa_bwd_strided pass N = Nq.  Returns 0 for
+ * invalid shapes.
  */
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
 
@@ -168,6 +169,31 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
            void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale, int causal,
            void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * fa_bwd_strided - fa_bwd with Nq query rows and Nk key rows per head and
+ * tensors in any layout whose head dimension is contiguous (the backward
+ * counterpart of fa_fwd_strided).  The causal mask keeps key j for query i
+ * when j <= i (top-left alignment, as fa_fwd_strided); with causal and
+ * Nk > Nq the key rows j >= Nq see no query, so their dK and dV are zero.
+ *
+ *   q, o, dout, dq : bf16, Nq rows per head.   k, v, dk, dv : bf16, Nk rows per head.
+ *   lse            : fp32 contiguous [B][H][Nq], the forward's L.
+ *   strides        : host pointer to 24 element strides, three per tensor in
+ *                    the order q, k, v, o, dout, dq, dk, dv; for each tensor
+ *                    {batch, head, row}: element (b, h, i, c) sits at
+ *                    b*s[0] + h*s[1] + i*s[2] + c.  Each stride >= 1 and
+ *                    < 2^38 (else FA_ERR_BAD_SHAPE) and a multiple of 8
+ *                    (16 bytes; else FA_ERR_MISALIGNED).  The caller keeps
+ *                    the three output tensors free of overlap with each other
+ *                    and with the inputs.
+ *   workspace      : at least fa_bwd_workspace_bytes(B, H, Nq, d) bytes.
+ *   Other arguments, checks and arithmetic as fa_bwd.
+ */
+int fa_bwd_strided(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                   const void* dout, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d,
+                   const long long* strides, float scale, int causal,
+                   void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * fa_fwd_noalloc - fa_fwd for callers that must not allocate device memory.

@@ -140,9 +140,11 @@ def test_backward_workspace_size_and_host_checks(lib):
 def test_backward_kernels_do_not_spill():
     if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
         pytest.skip("nvcc not available")
-    rep = build.ptxas_report({"fa_bwd_d32.cu", "fa_bwd_d64.cu", "fa_bwd_d128.cu"})
+    rep = build.ptxas_report({f"fa_bwd_d{d}{s}.cu" for d in (32, 64, 128) for s in ("", "_strided")})
     ks = {k: v for k, v in rep.items() if "fa_bwd" in k}
-    assert len(ks) == 15  # per head dimension: 4 tensor-core kernels and 1 preprocessing kernel
+    # per head dimension: 8 tensor-core kernels (dK/dV or dQ x causal or not x contiguous or
+    # strided) and 1 preprocessing kernel
+    assert len(ks) == 27
     for name, r in ks.items():
         assert r["spill_stores"] == 0 and r["spill_loads"] == 0, (name, r)
 
@@ -156,3 +158,28 @@ def test_strided_forward_rejects_bad_arguments_on_host(lib):
     assert fa.fa_fwd_strided(*[FAKE] * 5, 2, 3, 100, 0, 128, ok, ok, ok, ok, 0.1, 1, None) == -2
     assert fa.fa_fwd_strided(*[FAKE] * 5, 2, 3, 100, 70, 48, ok, ok, ok, ok, 0.1, 1, None) == -3
     assert fa.fa_fwd_strided(*[FAKE] * 4, 0, 2, 3, 100, 70, 128, ok, ok, ok, ok, 0.1, 1, None) == -1
+
+
+def test_strided_backward_rejects_bad_arguments_on_host(lib):
+    ok = (1 << 20, 1 << 14, 128)
+    st = [ok] * 8
+    r256 = lambda x: (x + 255) // 256 * 256
+    n = fa.fa_bwd_workspace_bytes(2, 3, 100, 128)       # sized by Nq = 100
+    assert n == 2 * r256(2 * 3 * 192 * 4)
+    ws = FAKE * 16
+    ptrs = [FAKE] * 9
+
+    def call(ptrs=ptrs, Nq=100, Nk=70, d=128, strides=st, scale=0.1, ws=ws, nbytes=n):
+        return fa.fa_bwd_strided(*ptrs, 2, 3, Nq, Nk, d, strides, scale, 1, ws, nbytes, None)
+
+    assert call(nbytes=n - 1) == -9                                   # workspace too small for Nq
+    assert call(Nq=300) == -9
+    assert call(strides=st[:5] + [(1 << 20, 1 << 14, 132)] + st[6:]) == -4   # dq row stride not 16-byte
+    assert call(strides=st[:6] + [(0, 8, 8)] + st[7:]) == -2          # dk batch stride 0
+    assert call(Nk=0) == -2
+    assert call(d=256) == -3
+    assert call(scale=float("nan")) == -8
+    assert call(ptrs=ptrs[:8] + [0]) == -1                            # dv missing
+    assert call(ptrs=ptrs[:2] + [FAKE + 4] + ptrs[3:]) == -4          # v not 16-byte aligned
+    with pytest.raises(ValueError):
+        fa.fa_bwd_strided(*ptrs, 2, 3, 100, 70, 128, st[:7], 0.1, 1, ws, n, None)

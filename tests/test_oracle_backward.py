@@ -225,3 +225,23 @@ def test_planted_backward_mistake_fails_a_pin(mutant):
             except Exception as e:  # a crash also counts as caught
                 failures.append(f"{pin.__name__} raised {type(e).__name__}")
     assert failures, f"no pin caught {mutant.__name__}"
+
+
+def test_backward_with_different_query_and_key_lengths():
+    """Nq != Nk (top-left causal alignment, as the forward): against torch fp64 autograd of its SDPA."""
+    rng = np.random.default_rng(23)
+    for nq, nk in ((3, 8), (8, 3), (1, 6), (7, 1), (33, 70)):
+        for causal in (False, True):
+            d = 4
+            q = rng.standard_normal((nq, d))
+            k = rng.standard_normal((nk, d)) * 1.5
+            v = rng.standard_normal((nk, d))
+            do = rng.standard_normal((nq, d))
+            scale = 0.8
+            dq, dk, dv = oracle.attention_backward_head(q, k, v, do, scale, causal)
+            tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+            o = torch.nn.functional.scaled_dot_product_attention(
+                tq[None, None], tk[None, None], tv[None, None], is_causal=causal, scale=scale)[0, 0]
+            o.backward(torch.from_numpy(do))
+            for mine, ref in ((dq, tq.grad), (dk, tk.grad), (dv, tv.grad)):
+                assert np.allclose(mine, ref.numpy(), atol=1e-11, rtol=0), (nq, nk, causal)

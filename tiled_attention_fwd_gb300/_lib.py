@@ -28,6 +28,8 @@ _SIGNATURES = {
     "fa_fwd_noalloc": (_c_int, [_c_void_p] * 5 + [_c_int] * 4 + [_c_float, _c_int, _c_void_p]),
     "fa_bwd_workspace_bytes": (_c_size_t, [_c_int] * 4),
     "fa_bwd": (_c_int, [_c_void_p] * 9 + [_c_int] * 4 + [_c_float, _c_int, _c_void_p, _c_size_t, _c_void_p]),
+    "fa_bwd_strided": (_c_int, [_c_void_p] * 9 + [_c_int] * 5 + [_c_void_p, _c_float, _c_int, _c_void_p, _c_size_t,
+                                                                  _c_void_p]),
     "fa_status": (_c_int, [_c_void_p]),
     "fa_set_wait_limit_ms": (_c_int, [_c_int]),
     "fa_strerror": (ctypes.c_char_p, [_c_int]),
@@ -132,6 +134,18 @@ def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal, workspa
                          workspace_bytes, stream)
 
 
+def fa_bwd_strided(q, k, v, o, lse, dout, dq, dk, dv, B, H, Nq, Nk, d, strides, scale, causal, workspace,
+                   workspace_bytes, stream) -> int:
+    """fa_bwd with Nq != Nk allowed; `strides` holds 8 {batch, head, row} element-stride triples
+    (q, k, v, o, dout, dq, dk, dv)."""
+    flat = [int(x) for st in strides for x in st]
+    if len(flat) != 24:
+        raise ValueError("strides must hold 8 triples")
+    arr = (ctypes.c_longlong * 24)(*flat)
+    return load().fa_bwd_strided(q, k, v, o, lse, dout, dq, dk, dv, B, H, Nq, Nk, d, ctypes.addressof(arr), scale,
+                                 int(bool(causal)), workspace, workspace_bytes, stream)
+
+
 def fa_status(stream) -> int:
     return load().fa_status(stream)
 
@@ -204,37 +218,63 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
     return o, l
 
 
-def backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None, workspace=None):
-    """dQ, dK, dV of the attention forward for bf16 CUDA tensors [B, H, N, d].
+def backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None, workspace=None,
+             out=None):
+    """dQ, dK, dV of the attention forward for bf16 CUDA tensors.
 
-    ``o`` and ``lse`` are the outputs of ``forward`` for the same q, k, v,
-    causal and scale; ``dout`` is the upstream gradient.  ``workspace`` (a
-    CUDA uint8 tensor of at least fa_bwd_workspace_bytes, 256-byte aligned) is
-    allocated here if not given.  Returns (dQ, dK, dV) in bf16.  Enqueued on
-    the current stream.
+    q, o, dout are [B, H, Nq, d] and k, v [B, H, Nk, d], in any layout whose
+    last dimension is contiguous; ``o`` and ``lse`` (fp32 contiguous
+    [B, H, Nq]) are the outputs of ``forward`` for the same q, k, v, causal
+    and scale; ``dout`` is the upstream gradient.  ``workspace`` (a CUDA uint8
+    tensor of at least fa_bwd_workspace_bytes(B, H, Nq, d), 256-byte aligned)
+    is allocated here if not given; so are the outputs unless ``out`` =
+    (dq, dk, dv) is given (shaped like q, k, v).  Returns (dQ, dK, dV) in
+    bf16.  Enqueued on the current stream.
     """
     import torch
 
+    if q.dim() != 4 or k.dim() != 4 or k.shape != v.shape or o.shape != q.shape or dout.shape != q.shape:
+        raise ValueError("q, o, dout must be [B, H, Nq, d] and k, v [B, H, Nk, d]")
+    if q.shape[:2] != k.shape[:2] or q.shape[3] != k.shape[3]:
+        raise ValueError("q, k, v must share B, H and d")
     ts = (q, k, v, o, dout)
-    if q.dim() != 4 or any(t.shape != q.shape for t in ts):
-        raise ValueError("q, k, v, o, dout must share the shape [B, H, N, d]")
-    if not all(t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous() for t in ts):
-        raise ValueError("q, k, v, o, dout must be contiguous bf16 CUDA tensors")
-    B, H, N, d = q.shape
-    if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_cuda:
-        raise ValueError("lse must be an fp32 CUDA tensor [B, H, N]")
+    if not all(t.is_cuda and t.dtype == torch.bfloat16 for t in ts):
+        raise ValueError("q, k, v, o, dout must be bf16 CUDA tensors")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if lse.shape != (B, H, Nq) or lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 CUDA tensor [B, H, Nq]")
     if scale is None:
         scale = d ** -0.5
-    need = fa_bwd_workspace_bytes(B, H, N, d)
+    need = fa_bwd_workspace_bytes(B, H, Nq, d)
     if workspace is None:
         workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    if out is None:
+        dq, dk, dv = (torch.empty(t.shape, device=t.device, dtype=t.dtype) for t in (q, k, v))
+    else:
+        dq, dk, dv = out
+        if dq.shape != q.shape or dk.shape != k.shape or dv.shape != v.shape or \
+                any(t.dtype != torch.bfloat16 or not t.is_cuda for t in out):
+            raise ValueError("out must be bf16 CUDA tensors shaped like q, k, v")
+    all_t = ts + (dq, dk, dv)
+    plain = Nq == Nk and all(t.is_contiguous() for t in all_t)
+    ws_bytes = workspace.numel() * workspace.element_size()
     with torch.cuda.device(q.device):
-        rc = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
-                    dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, float(scale), causal,
-                    workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-                    _stream_handle(torch, q.device))
-    _check(rc, "fa_bwd")
+        stream = _stream_handle(torch, q.device)
+        if plain:
+            rc = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
+                        dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Nq, d, float(scale), causal,
+                        workspace.data_ptr(), ws_bytes, stream)
+            name = "fa_bwd"
+        else:
+            if any(t.stride(3) != 1 for t in all_t):
+                raise ValueError("the last dimension of every tensor must be contiguous")
+            rc = fa_bwd_strided(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Nq, Nk, d,
+                                [t.stride()[:3] for t in all_t], float(scale), causal, workspace.data_ptr(),
+                                ws_bytes, stream)
+            name = "fa_bwd_strided"
+    _check(rc, name)
     return dq, dk, dv
 
 

@@ -366,22 +366,45 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
   return 2 * fa::round256(static_cast<size_t>(B) * H * n_pad * 4);
 }
 
+namespace fa {
+namespace {
+
+// Checks shared by fa_bwd and fa_bwd_strided, then the launch.  The strides in
+// a.st are already validated by the caller; `strided` selects the 4-D maps.
+int run_bwd(BwdArgs& a, int d, bool strided, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!a.q || !a.k || !a.v || !a.o || !a.lse || !a.dout || !a.dq || !a.dk || !a.dv || !workspace)
+    return FA_ERR_NULL_POINTER;
+  if (!aligned16(a.q) || !aligned16(a.k) || !aligned16(a.v) || !aligned16(a.o) || !aligned16(a.dout) ||
+      !aligned16(a.dq) || !aligned16(a.dk) || !aligned16(a.dv) || (reinterpret_cast<uintptr_t>(a.lse) & 3u) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return FA_ERR_MISALIGNED;
+  if (workspace_bytes < fa_bwd_workspace_bytes(a.B, a.H, a.Nq, d)) return FA_ERR_WORKSPACE;
+  DeviceState* s = nullptr;
+  int rc = current_device_state(&s);
+  if (rc != FA_OK) return rc;
+  const LaunchCtx ctx = make_ctx(*s, stream);
+  a.n_pad = (a.Nq + 191) / 192 * 192;
+  a.l2 = static_cast<float*>(workspace);
+  a.dsum = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                    round256(static_cast<size_t>(a.B) * a.H * a.n_pad * 4));
+  int e = 0;
+  switch (d) {
+    case 32: e = strided ? launch_bwd_strided_d32(a, ctx) : launch_bwd_d32(a, ctx); break;
+    case 64: e = strided ? launch_bwd_strided_d64(a, ctx) : launch_bwd_d64(a, ctx); break;
+    default: e = strided ? launch_bwd_strided_d128(a, ctx) : launch_bwd_d128(a, ctx); break;
+  }
+  return e == 0 ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace fa
+
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout, void* dq,
            void* dk, void* dv, int B, int H, int N, int d, float scale, int causal, void* workspace,
            size_t workspace_bytes, void* stream) {
-  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace) return FA_ERR_NULL_POINTER;
   int rc = fa::check_common(B, H, N, d, scale);
   if (rc != FA_OK) return rc;
   if (d != 32 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED_D;
-  if (!fa::aligned16(q) || !fa::aligned16(k) || !fa::aligned16(v) || !fa::aligned16(o) || !fa::aligned16(dout) ||
-      !fa::aligned16(dq) || !fa::aligned16(dk) || !fa::aligned16(dv) || (reinterpret_cast<uintptr_t>(lse) & 3u) ||
-      (reinterpret_cast<uintptr_t>(workspace) & 255u))
-    return FA_ERR_MISALIGNED;
-  if (workspace_bytes < fa_bwd_workspace_bytes(B, H, N, d)) return FA_ERR_WORKSPACE;
-  fa::DeviceState* s = nullptr;
-  rc = fa::current_device_state(&s);
-  if (rc != FA_OK) return rc;
-  const fa::LaunchCtx ctx = fa::make_ctx(*s, stream);
   fa::BwdArgs a;
   a.q = q;
   a.k = k;
@@ -392,21 +415,48 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;
-  a.BH = B * H;
-  a.N = N;
-  a.n_pad = (N + 191) / 192 * 192;
+  a.B = B;
+  a.H = H;
+  a.Nq = N;
+  a.Nk = N;
+  for (auto& st : a.st) fa::contiguous_strides(st, H, N, d);
   a.scale = scale;
   a.causal = causal != 0;
-  a.l2 = static_cast<float*>(workspace);
-  a.dsum = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                    fa::round256(static_cast<size_t>(a.BH) * a.n_pad * 4));
-  int e = 0;
-  switch (d) {
-    case 32: e = fa::launch_bwd_d32(a, ctx); break;
-    case 64: e = fa::launch_bwd_d64(a, ctx); break;
-    default: e = fa::launch_bwd_d128(a, ctx); break;
-  }
-  return e == 0 ? FA_OK : FA_ERR_CUDA;
+  return fa::run_bwd(a, d, false, workspace, workspace_bytes, stream);
+}
+
+int fa_bwd_strided(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                   void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, const long long* strides,
+                   float scale, int causal, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!strides) return FA_ERR_NULL_POINTER;
+  int rc = fa::check_common(B, H, Nq, d, scale);
+  if (rc != FA_OK) return rc;
+  rc = fa::check_common(B, H, Nk, d, scale);
+  if (rc != FA_OK) return rc;
+  if (d != 32 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED_D;
+  for (int i = 0; i < 24; ++i)
+    if (strides[i] < 1 || strides[i] >= (1LL << 38)) return FA_ERR_BAD_SHAPE;
+  for (int i = 0; i < 24; ++i)
+    if (strides[i] % 8 != 0) return FA_ERR_MISALIGNED;  // 16-byte rows and tiles (TMA, vector loads and stores)
+  fa::BwdArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.dout = dout;
+  a.lse = lse;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.B = B;
+  a.H = H;
+  a.Nq = Nq;
+  a.Nk = Nk;
+  for (int t = 0; t < 8; ++t)
+    for (int i = 0; i < 3; ++i) a.st[t][i] = strides[3 * t + i];
+  a.scale = scale;
+  a.causal = causal != 0;
+  return fa::run_bwd(a, d, true, workspace, workspace_bytes, stream);
 }
 
 int fa_status(void* stream) {

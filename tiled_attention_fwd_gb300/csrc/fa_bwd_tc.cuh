@@ -34,7 +34,9 @@
 namespace fa {
 
 struct BwdParams {
-  int N;                 // sequence length
+  int Nq;                // query rows per head
+  int Nk;                // key / value rows per head
+  int H;                 // heads (unit index bh = b * H + h)
   int BH;                // batch * heads
   int n_pad;             // row stride of the l2 / dsum vectors: N rounded up to 192 (a multiple of every BS)
   int n_m;               // 128-row tiles of the fixed operands per head: ceil(N / 128)
@@ -44,8 +46,10 @@ struct BwdParams {
   float scale_log2;      // scale * log2(e)
   const float* l2;       // [BH][n_pad]: L * log2(e); +inf on rows >= N
   const float* dsum;     // [BH][n_pad]: D = rowsum(dO * O); 0 on rows >= N
-  __nv_bfloat16* out0;   // MODE 0: dK, MODE 1: dQ   [BH][N][D]
-  __nv_bfloat16* out1;   // MODE 0: dV
+  __nv_bfloat16* out0;   // MODE 0: dK, MODE 1: dQ: contiguous [BH][rows][D], or (strided
+  __nv_bfloat16* out1;   // MODE 0: dV               kernels) row i of (b, h) at b*s[0] + h*s[1] + i*s[2]
+  long long out0_s[3];   // element strides {batch, head, row} of out0 / out1 (strided kernels)
+  long long out1_s[3];
   int* status;           // device status word
   unsigned long long limit_ns;
 };
@@ -125,6 +129,7 @@ __device__ __forceinline__ BwdUnit bwd_decode(int u, const BwdParams& p) {
     const int last = (w.m0 + 127) / BwdCfg<D, MODE>::BS + 1;  // key tiles holding some key <= the last query
     w.s_end = (CAUSAL && last < p.n_s) ? last : p.n_s;
   }
+  if (w.s_begin > w.s_end) w.s_begin = w.s_end;  // MODE 0, causal, keys past the last query: no tile
   return w;
 }
 
@@ -172,7 +177,7 @@ __device__ __forceinline__ bool bwd_wait_drain(uint32_t bar, uint32_t parity, co
 // stage per streamed tile: B1 and B2 (BS rows each) and, in MODE 0, the 64
 // streamed rows' L * log2(e) and D.
 //   MODE 0: A1 = K, A2 = V, B1 = Q, B2 = dO.   MODE 1: A1 = Q, A2 = dO, B1 = K, B2 = V.
-template <int D, int MODE, bool CAUSAL>
+template <int D, int MODE, bool CAUSAL, bool STRIDED>
 __device__ __forceinline__ void bwd_producer(const CUtensorMap* tm_a1, const CUtensorMap* tm_a2,
                                              const CUtensorMap* tm_b1, const CUtensorMap* tm_b2, const BwdParams& p,
                                              const BwdBars<D, MODE>& bar, uint32_t base, const WaitGuard& g) {
@@ -188,10 +193,17 @@ __device__ __forceinline__ void bwd_producer(const CUtensorMap* tm_a1, const CUt
     const BwdUnit w = bwd_decode<D, MODE, CAUSAL>(u, p);
     if (!(ok = wait_bar(bar.fix_empty(), (uk & 1) ^ 1, g, kStatusTimeoutLoad))) break;
     mbar_arrive_expect_tx(bar.fix_full(), 2 * C::FIX_TILE);
+    // Strided tensors are 4-D maps {d, rows, H, B}; contiguous ones 3-D {d, rows, B*H}.
+    const int th = STRIDED ? w.bh % p.H : w.bh, tb = STRIDED ? w.bh / p.H : 0;
+    auto load = [&](uint32_t dst, const CUtensorMap* tm, uint32_t full, int x, int row, uint64_t pol) {
+      if constexpr (STRIDED)
+        tma_load_4d(dst, tm, full, x, row, th, tb, pol);
+      else
+        tma_load_3d(dst, tm, full, x, row, th, pol);
+    };
     for (int r = 0; r < C::NR; ++r) {
-      tma_load_3d(base + C::OFF_FIX + r * C::FIX_REGION, tm_a1, bar.fix_full(), r * C::RC, w.m0, w.bh, pol_fix);
-      tma_load_3d(base + C::OFF_FIX + C::FIX_TILE + r * C::FIX_REGION, tm_a2, bar.fix_full(), r * C::RC, w.m0, w.bh,
-                  pol_fix);
+      load(base + C::OFF_FIX + r * C::FIX_REGION, tm_a1, bar.fix_full(), r * C::RC, w.m0, pol_fix);
+      load(base + C::OFF_FIX + C::FIX_TILE + r * C::FIX_REGION, tm_a2, bar.fix_full(), r * C::RC, w.m0, pol_fix);
     }
     last_fix = uk;
     for (int s = w.s_begin; s < w.s_end; ++s) {
@@ -202,8 +214,8 @@ __device__ __forceinline__ void bwd_producer(const CUtensorMap* tm_a1, const CUt
       const uint32_t full = bar.st_full(st);
       mbar_arrive_expect_tx(full, 2 * C::S_TILE + (C::KV ? 2 * C::VEC_BYTES : 0));
       for (int r = 0; r < C::NR; ++r) {
-        tma_load_3d(s0 + r * C::S_REGION, tm_b1, full, r * C::RC, s * C::BS, w.bh, pol_str);
-        tma_load_3d(s0 + C::S_TILE + r * C::S_REGION, tm_b2, full, r * C::RC, s * C::BS, w.bh, pol_str);
+        load(s0 + r * C::S_REGION, tm_b1, full, r * C::RC, s * C::BS, pol_str);
+        load(s0 + C::S_TILE + r * C::S_REGION, tm_b2, full, r * C::RC, s * C::BS, pol_str);
       }
       if constexpr (C::KV) {
         // s * BS + BS <= n_pad (a multiple of BS), and BS * 4 is a multiple of 16: aligned, in bounds.
@@ -304,6 +316,19 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, const BwdBars<D, MOD
     const int n = w.s_end - w.s_begin;
     if (!(ok = wait(bar.fix_full(), uk & 1))) break;
     tc_fence_after();
+    if (n <= 0) {
+      // No streamed tile reaches these fixed rows (MODE 0, causal, with more
+      // keys than queries): nothing to multiply; the epilogue writes zeros.
+      // The previous unit's epilogue must still release the accumulators
+      // first, so that each out_free phase collects the arrivals of one unit.
+      if (uk > 0) {
+        if (!(ok = wait(bar.out_free(), (uk - 1) & 1))) break;
+        tc_fence_after();
+      }
+      mma_commit_elect(bar.fix_empty());
+      mma_commit_elect(bar.out_done());
+      continue;
+    }
     auto stage_of = [&](int t) -> uint32_t { return (pos + t) % C::NST; };
     auto acquire = [&](int t) -> bool {
       const uint32_t q = pos + t;
@@ -353,7 +378,7 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, const BwdBars<D, MOD
 // it is the A operand of dV).  At the end of each unit both warpgroups read the
 // accumulators out (MODE 0: warpgroup 0 dK, warpgroup 1 dV; MODE 1: dQ, split
 // by 32-column chunks) and release them.
-template <int D, int MODE, bool CAUSAL>
+template <int D, int MODE, bool CAUSAL, bool STRIDED>
 __device__ __forceinline__ void bwd_elementwise(const BwdParams& p, const BwdBars<D, MODE>& bar, uint8_t* gbase,
                                                 uint32_t tmem, int b, int quarter, int lane, const WaitGuard& g) {
   using C = BwdCfg<D, MODE>;
@@ -390,7 +415,7 @@ __device__ __forceinline__ void bwd_elementwise(const BwdParams& p, const BwdBar
       if (MODE == 0)
         need_mask = CAUSAL && col0 < w.m0 + C::BM - 1;
       else
-        need_mask = (col0 + C::BS > p.N) || (CAUSAL && col0 + C::BS - 1 > w.m0);
+        need_mask = (col0 + C::BS > p.Nk) || (CAUSAL && col0 + C::BS - 1 > w.m0);
       const float4* vl2 = reinterpret_cast<const float4*>(gbase + C::OFF_ST + st * C::STAGE + 2 * C::S_TILE);
       const float4* vd = vl2 + C::BS / 4;
       // Two chunks of 32 streamed rows: load S and dP, form P and dS, store
@@ -424,7 +449,7 @@ __device__ __forceinline__ void bwd_elementwise(const BwdParams& p, const BwdBar
             float pe = ex2(fmaf(__uint_as_float(rs[c]), sl2, -l2c[e]));
             if (need_mask) {
               const int col = col0 + h * 32 + c;
-              const bool masked = (MODE == 0) ? (CAUSAL && row > col) : (col >= p.N || (CAUSAL && col > row));
+              const bool masked = (MODE == 0) ? (CAUSAL && row > col) : (col >= p.Nk || (CAUSAL && col > row));
               if (masked) pe = 0.f;
             }
             pv[e] = pe;
@@ -456,20 +481,32 @@ __device__ __forceinline__ void bwd_elementwise(const BwdParams& p, const BwdBar
     __nv_bfloat16* out = second ? p.out1 : p.out0;
     const float f = second ? 1.f : p.scale;  // dK and dQ carry the softmax scale
     const uint64_t f2 = f2_pack(f, f);
-    __nv_bfloat16* orow = out + (static_cast<size_t>(w.bh) * p.N + row) * D;
+    const int n_rows = (MODE == 0) ? p.Nk : p.Nq;  // rows of the fixed operand (and of the outputs)
+    __nv_bfloat16* orow;
+    if constexpr (STRIDED) {
+      const long long* os = second ? p.out1_s : p.out0_s;
+      orow = out + (w.bh / p.H) * os[0] + (w.bh % p.H) * os[1] + static_cast<long long>(row) * os[2];
+    } else {
+      orow = out + (static_cast<size_t>(w.bh) * n_rows + row) * D;
+    }
+    const bool empty = n <= 0;  // no streamed tile reached these rows: the gradients are zero
 #pragma unroll 1
     for (int c = 0; c < D / 32; ++c) {
       if (!C::KV && (c & 1) != b) continue;
       uint32_t v[32];
       tmem_ld32(acc + c * 32, v);
       tmem_wait_ld(v);
+      if (empty) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0u;
+      }
       uint32_t packed[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const float2 y = f2_unpack(f2_mul(f2_pack(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), f2));
         packed[i] = pack_bf16x2(y.x, y.y);
       }
-      if (row < p.N) {
+      if (row < n_rows) {
         uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
@@ -482,7 +519,7 @@ __device__ __forceinline__ void bwd_elementwise(const BwdParams& p, const BwdBar
 }
 
 // ------------------------------------------------------------------ kernel
-template <int D, int MODE, bool CAUSAL>
+template <int D, int MODE, bool CAUSAL, bool STRIDED>
 __global__ void __launch_bounds__(BwdCfg<D, MODE>::THREADS, 1)
     fa_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_a1, const __grid_constant__ CUtensorMap tm_a2,
                      const __grid_constant__ CUtensorMap tm_b1, const __grid_constant__ CUtensorMap tm_b2,
@@ -532,11 +569,11 @@ __global__ void __launch_bounds__(BwdCfg<D, MODE>::THREADS, 1)
   const WaitGuard g{abort_flag, p.status, p.limit_ns};
 
   if (warp < 8) {
-    bwd_elementwise<D, MODE, CAUSAL>(p, bar, gbase, tmem, warp >> 2, warp & 3, lane, g);
+    bwd_elementwise<D, MODE, CAUSAL, STRIDED>(p, bar, gbase, tmem, warp >> 2, warp & 3, lane, g);
   } else if (warp == C::MMA_WARP) {
     bwd_mma<D, MODE, CAUSAL>(p, bar, base, tmem, g);
   } else if (warp == C::LOAD_WARP && lane == 0) {
-    bwd_producer<D, MODE, CAUSAL>(&tm_a1, &tm_a2, &tm_b1, &tm_b2, p, bar, base, g);
+    bwd_producer<D, MODE, CAUSAL, STRIDED>(&tm_a1, &tm_a2, &tm_b1, &tm_b2, p, bar, base, g);
   }
 
   __syncwarp();
@@ -550,13 +587,21 @@ __global__ void __launch_bounds__(BwdCfg<D, MODE>::THREADS, 1)
 
 // ------------------------------------------------------------------ preprocessing
 // D[row] = sum_c dO[row, c] * O[row, c] (fp32) and l2[row] = L[row] * log2(e),
-// for rows [0, n_pad) of every head; rows >= N get D = 0 and l2 = +inf, so
-// their P is exactly 0.  Each row is read by D / 8 lanes, 16 bytes per lane.
+// for query rows [0, n_pad) of every head (N = the query rows; O and dO are
+// read through their strides, L is contiguous [BH][N]); rows >= N get D = 0
+// and l2 = +inf, so their P is exactly 0.  Each row is read by D / 8 lanes,
+// 16 bytes per lane.
+struct PrepStrides {
+  long long o[3];   // element strides {batch, head, row} of O
+  long long d[3];   // ... of dO
+};
+
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
                                                           const __nv_bfloat16* __restrict__ dout,
                                                           const float* __restrict__ lse, float* __restrict__ l2,
-                                                          float* __restrict__ dsum, int BH, int N, int n_pad) {
+                                                          float* __restrict__ dsum, int BH, int H, int N, int n_pad,
+                                                          const PrepStrides st) {
   constexpr int CPR = D / 8;            // 16-byte chunks per row
   constexpr int RPW = 32 / CPR;         // rows per warp step
   const int lane = threadIdx.x & 31;
@@ -571,9 +616,11 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __nv_bfloat16* _
     const bool valid = rr < total && i < N;
     float acc = 0.f;
     if (valid) {
-      const size_t off = (static_cast<size_t>(bh) * N + i) * D + chunk * 8;
-      const uint4 a = *reinterpret_cast<const uint4*>(o + off);
-      const uint4 c = *reinterpret_cast<const uint4*>(dout + off);
+      const long long hb = bh / H, hh = bh % H;
+      const long long oo = hb * st.o[0] + hh * st.o[1] + i * st.o[2] + chunk * 8;
+      const long long od = hb * st.d[0] + hh * st.d[1] + i * st.d[2] + chunk * 8;
+      const uint4 a = *reinterpret_cast<const uint4*>(o + oo);
+      const uint4 c = *reinterpret_cast<const uint4*>(dout + od);
       const uint32_t av[4] = {a.x, a.y, a.z, a.w}, cv[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {

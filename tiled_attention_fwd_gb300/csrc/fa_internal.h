@@ -78,8 +78,12 @@ int launch_tc_strided_d64(const FwdArgs& a, const LaunchCtx& ctx);
 int launch_tc_strided_d128(const FwdArgs& a, const LaunchCtx& ctx);
 int launch_tc_strided_d256(const FwdArgs& a, const LaunchCtx& ctx);
 
-// Arguments of the backward pass (device pointers; bf16 tensors [BH][N][d],
-// lse fp32 [BH][N]; l2 and dsum are workspace vectors [BH][n_pad]).
+// Arguments of the backward pass (device pointers).  The bf16 tensors q, o,
+// dout, dq have Nq rows per head, k, v, dk, dv Nk rows; tensor t's row i of
+// (b, h) starts at element b * st[t][0] + h * st[t][1] + i * st[t][2] (the
+// head dimension contiguous), t = 0 q, 1 k, 2 v, 3 o, 4 dout, 5 dq, 6 dk, 7 dv.
+// lse is fp32 contiguous [B][H][Nq]; l2 and dsum are workspace vectors
+// [B*H][n_pad].
 struct BwdArgs {
   const void* q;
   const void* k;
@@ -90,9 +94,12 @@ struct BwdArgs {
   void* dq;
   void* dk;
   void* dv;
-  int BH;
-  int N;
-  int n_pad;       // N rounded up to a multiple of 192
+  int B;
+  int H;
+  int Nq;
+  int Nk;
+  long long st[8][3];
+  int n_pad;       // Nq rounded up to a multiple of 192
   float scale;
   bool causal;
   float* l2;
@@ -104,6 +111,10 @@ struct BwdArgs {
 int launch_bwd_d32(const BwdArgs& a, const LaunchCtx& ctx);
 int launch_bwd_d64(const BwdArgs& a, const LaunchCtx& ctx);
 int launch_bwd_d128(const BwdArgs& a, const LaunchCtx& ctx);
+// The same for strided tensors (4-D tensor maps).  Defined in fa_bwd_d<D>_strided.cu.
+int launch_bwd_strided_d32(const BwdArgs& a, const LaunchCtx& ctx);
+int launch_bwd_strided_d64(const BwdArgs& a, const LaunchCtx& ctx);
+int launch_bwd_strided_d128(const BwdArgs& a, const LaunchCtx& ctx);
 
 // The bf16 forward for d in {32, 64, 128, 256}; takes the contiguous kernels
 // when every tensor is contiguous [B][H][N][d], else the strided ones; returns
