@@ -17,7 +17,10 @@
 //     arithmetic, write P as bf16 over S in TMEM, keep m and l;
 //   * a correction warpgroup: rescales the O accumulators in TMEM by alpha
 //     while the softmax computes P, and runs the epilogue (O / l in bf16,
-//     L = m + log l) so the softmax can start the next work unit at once;
+//     L = m + log l) so the softmax can start the next work unit at once; each
+//     warp stages its 32 rows of O in shared memory, 32 columns at a time, and
+//     a TMA store writes them out, so O is free for the next unit as soon as
+//     it has been read;
 //   * one MMA warp: tcgen05.mma S = Q K^T into TMEM, then O += P V with P read
 //     from TMEM and V from shared memory, issued by an elected lane;
 //   * one TMA producer warp: Q tiles and a ring of K/V stages in 128-byte
@@ -55,9 +58,11 @@ struct TcParams {
   int n_qb;              // query blocks per head: ceil(N / (BQ * NQT))
   int total_units;       // BH * n_qb
   float scale_log2;      // softmax scale * log2(e)
-  __nv_bfloat16* o;      // O(b, h, row, :): contiguous [BH][Nq][D], or (strided kernels)
-  long long o_sb, o_sh, o_sn;  // at o + b * o_sb + h * o_sh + row * o_sn (the d dimension contiguous)
   float* lse;            // [BH][Nq], contiguous
+  // O(b, h, row, :) at o + b * o_sb + h * o_sh + row * o_sn (d contiguous); the
+  // kernels with EPI_TMA write it through its tensor map instead.
+  __nv_bfloat16* o;
+  long long o_sb, o_sh, o_sn;
   int* status;           // device status word
   unsigned long long limit_ns;  // time limit of each device-side wait
 };
@@ -82,7 +87,15 @@ struct TcCfg {
   static constexpr int SMEM_LIMIT = 227 * 1024;
   // A K/V stage holds two tiles: V_j and K_{j+LA} (the first stage of a unit: K_0 .. K_{LA-1}).
   static constexpr int STAGE = 2 * KV_TILE;
-  static constexpr int NST_FIT = (SMEM_LIMIT - 1024 - MISC - NQT * Q_TILE) / STAGE;
+  // Epilogue staging: per correction warp OSTB buffers of 32 rows x 32 bf16
+  // columns (64-byte swizzled), the source boxes of the TMA stores of O.
+  // d = 64 keeps direct 16-byte stores from registers: there the staged
+  // stores measured slower.
+  static constexpr bool EPI_TMA = (D != 64);
+  static constexpr int OSTB = 3;
+  static constexpr int OST_BUF = 32 * 64;
+  static constexpr int OST = EPI_TMA ? 4 * OSTB * OST_BUF : 0;
+  static constexpr int NST_FIT = (SMEM_LIMIT - 1024 - MISC - OST - NQT * Q_TILE) / STAGE;
   static constexpr int NST = NST_FIT > 4 ? 4 : NST_FIT;  // K/V stages
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = NQT * Q_TILE;
@@ -96,7 +109,8 @@ struct TcCfg {
   static constexpr int OFF_STAT_L = OFF_STAT_M + 4 * 128 * 4; // float [2][NO][128]
   static constexpr int OFF_TMEM_SLOT = OFF_STAT_L + 4 * 128 * 4;
   static constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
-  static constexpr int SMEM_USED = OFF_MISC + MISC + 1024;    // + slack for 1024-byte alignment
+  static constexpr int OFF_OST = OFF_MISC + MISC;             // 1024-byte aligned
+  static constexpr int SMEM_USED = OFF_OST + OST + 1024;      // + slack for 1024-byte alignment
   // At least ~120 KB so that a second CTA never shares the SM (and its TMEM).
   static constexpr int SMEM_ALLOC = SMEM_USED < 120 * 1024 ? 120 * 1024 : SMEM_USED;
   // TMEM columns.  S/P buffer b at TM_S + b*128, O accumulator t at TM_O + t*D.
@@ -580,10 +594,17 @@ __device__ __forceinline__ void tc_softmax(const TcParams& p, const TcBars<D>& b
       const int key0 = j * C::BK;
       const bool need_mask = (CAUSAL && key0 + C::BK - 1 > row0) || (key0 + C::BK > p.Nk);
       if (need_mask) {
+        // Column c of this row is visible iff c <= lim; 32-column blocks that
+        // every lane of the warp sees whole are skipped (warp-uniform test).
+        const int lim = (CAUSAL ? min(row, p.Nk - 1) : p.Nk - 1) - key0;
+        const int lo = __reduce_min_sync(0xffffffffu, lim);
 #pragma unroll
-        for (int c = 0; c < C::BK; ++c) {
-          const int key = key0 + c;
-          if (key >= p.Nk || (CAUSAL && key > row)) s[c] = -INFINITY;
+        for (int cb = 0; cb < C::BK / 32; ++cb) {
+          if (32 * cb + 31 > lo) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (32 * cb + i > lim) s[32 * cb + i] = -INFINITY;
+          }
         }
       }
       // Row max: 8 chains of three-input maxima over interleaved columns.
@@ -644,8 +665,9 @@ __device__ __forceinline__ void tc_softmax(const TcParams& p, const TcBars<D>& b
 
 // ------------------------------------------------------------------ correction + epilogue
 template <int D, bool CAUSAL, bool STRIDED>
-__device__ __forceinline__ void tc_correction(const TcParams& p, const TcBars<D>& bar, uint8_t* gbase, uint32_t tmem,
-                                              int quarter, int lane, const WaitGuard& g) {
+__device__ __forceinline__ void tc_correction(const TcParams& p, const CUtensorMap* tm_o, const TcBars<D>& bar,
+                                              uint8_t* gbase, uint32_t tmem, int quarter, int lane,
+                                              const WaitGuard& g) {
   using C = TcCfg<D>;
   const int r = quarter * 32 + lane;
   const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
@@ -702,7 +724,15 @@ __device__ __forceinline__ void tc_correction(const TcParams& p, const TcBars<D>
     release_o(t);
     return true;
   };
-  // Epilogue of accumulator t: O / l in bf16, L = (m + log2 l) * ln 2; then O is free again.
+  // Epilogue of accumulator t: O / l in bf16, L = (m + log2 l) * ln 2.  This
+  // warp's 32 rows go out 32 columns at a time: TMEM -> registers -> a staging
+  // buffer in shared memory (64-byte swizzle: 16-byte unit k of row i at unit
+  // k ^ ((i >> 1) & 3), so a warp's stores hit every bank once) -> TMA store
+  // issued by lane 0.  O is released to the next unit right after its last
+  // TMEM read; a buffer is rewritten only once the store that read it three
+  // chunks earlier has finished reading.
+  const uint32_t ost = smem_u32(gbase + C::OFF_OST) + static_cast<uint32_t>(quarter * C::OSTB * C::OST_BUF);
+  uint32_t ost_n = 0;  // chunks staged by this warp so far
   auto epilogue = [&](const TcUnit& w, int su, int t, uint32_t& od, uint32_t& lf) -> bool {
     bool k = warp_wait_bar(bar.o_done(t), od & 1, g, kStatusTimeoutSoftmax);
     k = k && warp_wait_bar(bar.l_full(t), lf & 1, g, kStatusTimeoutSoftmax);
@@ -715,24 +745,49 @@ __device__ __forceinline__ void tc_correction(const TcParams& p, const TcBars<D>
     const float inv_l = 1.f / lrow;
     const uint64_t il2 = f2_pack(inv_l, inv_l);
     const int row = w.row0 + t * C::BQ + r;
+    const int wrow0 = w.row0 + t * C::BQ + quarter * 32;  // first row of this warp's box
     const uint32_t to = tmem + lane_off + C::TM_O + t * D;
-    __nv_bfloat16* orow;
-    if constexpr (STRIDED)
-      orow = p.o + (w.bh / p.H) * p.o_sb + (w.bh % p.H) * p.o_sh + static_cast<long long>(row) * p.o_sn;
-    else
-      orow = p.o + (static_cast<size_t>(w.bh) * p.Nq + row) * D;
+    const uint32_t sw = static_cast<uint32_t>((lane >> 1) & 3);
 #pragma unroll 1
     for (int c = 0; c < D / 32; ++c) {
       uint32_t v[32];
       tmem_ld32(to + c * 32, v);
       tmem_wait_ld(v);
+      if (c == D / 32 - 1) {
+        tc_fence_before();
+        release_o(t);  // O may be overwritten by the next unit's first P V
+      }
       uint32_t packed[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const float2 y = f2_unpack(f2_mul(f2_pack(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), il2));
         packed[i] = pack_bf16x2(y.x, y.y);
       }
-      if (row < p.Nq) {
+      if constexpr (C::EPI_TMA) {
+        const uint32_t buf = ost + (ost_n % C::OSTB) * C::OST_BUF;
+        ++ost_n;
+        if (lane == 0) bulk_wait_group_read<C::OSTB - 1>();
+        __syncwarp();
+        const uint32_t rb = buf + static_cast<uint32_t>(lane) * 64;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          st_shared_v4(rb + ((static_cast<uint32_t>(u) ^ sw) << 4), packed[4 * u], packed[4 * u + 1],
+                       packed[4 * u + 2], packed[4 * u + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && wrow0 < p.Nq) {
+          if constexpr (STRIDED)
+            tma_store_4d(tm_o, buf, c * 32, wrow0, w.bh % p.H, w.bh / p.H);
+          else
+            tma_store_3d(tm_o, buf, c * 32, wrow0, w.bh);
+          bulk_commit_group();
+        }
+      } else if (row < p.Nq) {
+        __nv_bfloat16* orow;
+        if constexpr (STRIDED)
+          orow = p.o + (w.bh / p.H) * p.o_sb + (w.bh % p.H) * p.o_sh + static_cast<long long>(row) * p.o_sn;
+        else
+          orow = p.o + (static_cast<size_t>(w.bh) * p.Nq + row) * D;
         uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
@@ -740,8 +795,6 @@ __device__ __forceinline__ void tc_correction(const TcParams& p, const TcBars<D>
       }
     }
     if (row < p.Nq) p.lse[static_cast<size_t>(w.bh) * p.Nq + row] = (mrow + log2f(lrow)) * 0.69314718055994531f;
-    tc_fence_before();
-    release_o(t);  // O may be overwritten by the next unit's first P V
     return true;
   };
 
@@ -758,13 +811,17 @@ __device__ __forceinline__ void tc_correction(const TcParams& p, const TcBars<D>
       if (C::NO == 2 && ok && j == w.n[1] - 1) ok = epilogue(w, uk & 1, 1, od1, lf1);
     }
   }
+  // The staged O tiles must be written (and their shared memory read) before the CTA exits.
+  if (C::EPI_TMA && lane == 0) bulk_wait_group_all();
+  __syncwarp();
 }
 
 // ------------------------------------------------------------------ kernel
 template <int D, bool CAUSAL, bool STRIDED>
 __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
     fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                     const TcParams p) {
   using C = TcCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -803,6 +860,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
+    prefetch_tmap(&tm_o);
   }
   if (warp == C::MMA_WARP) {
     tmem_alloc(smem_u32(tmem_slot), C::TM_COLS);
@@ -819,7 +877,7 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
     tc_softmax<D, CAUSAL>(p, bar, gbase, tmem, warp >> 2, warp & 3, lane, g);
   } else if (warp < C::SOFTMAX_WARPS + 4) {
     if constexpr (C::SPLIT_REGS) regs_decrease<C::reg_corr(STRIDED)>();
-    tc_correction<D, CAUSAL, STRIDED>(p, bar, gbase, tmem, warp & 3, lane, g);
+    tc_correction<D, CAUSAL, STRIDED>(p, &tm_o, bar, gbase, tmem, warp & 3, lane, g);
   } else {
     if constexpr (C::SPLIT_REGS) regs_decrease<C::REG_CORR_OTHER - C::reg_corr(STRIDED)>();
     if (warp == C::LOAD_WARP && lane == 0) tc_producer<D, CAUSAL, STRIDED>(&tm_q, &tm_k, &tm_v, p, bar, base, g);

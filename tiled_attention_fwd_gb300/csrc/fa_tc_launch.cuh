@@ -30,15 +30,18 @@ int launch_tc_impl(const FwdArgs& a, const LaunchCtx& ctx) {
   // The attribute is per function and device; setting it again is cheap and idempotent.
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
   if (e != cudaSuccess) return static_cast<int>(e);
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
+  // O is stored in boxes of 32 rows x 32 columns (one correction warp, one chunk), 64-byte swizzle.
   if constexpr (STRIDED) {
     if (encode_bf16_map4(&mq, a.q, a.B, a.H, a.Nq, D, a.qs, C::RC, C::BQ, C::SWB) != 0) return -1;
     if (encode_bf16_map4(&mk, a.k, a.B, a.H, a.Nk, D, a.ks, C::RC, C::BK, C::SWB) != 0) return -1;
     if (encode_bf16_map4(&mv, a.v, a.B, a.H, a.Nk, D, a.vs, C::RC, C::BK, C::SWB) != 0) return -1;
+    if (encode_bf16_map4(&mo, a.o, a.B, a.H, a.Nq, D, a.os, 32, 32, 64) != 0) return -1;
   } else {
     if (encode_bf16_map(&mq, a.q, a.B * a.H, a.Nq, D, C::RC, C::BQ, C::SWB) != 0) return -1;
     if (encode_bf16_map(&mk, a.k, a.B * a.H, a.Nk, D, C::RC, C::BK, C::SWB) != 0) return -1;
     if (encode_bf16_map(&mv, a.v, a.B * a.H, a.Nk, D, C::RC, C::BK, C::SWB) != 0) return -1;
+    if (encode_bf16_map(&mo, a.o, a.B * a.H, a.Nq, D, 32, 32, 64) != 0) return -1;
   }
   TcParams p;
   p.Nq = a.Nq;
@@ -49,15 +52,15 @@ int launch_tc_impl(const FwdArgs& a, const LaunchCtx& ctx) {
   p.n_qb = (a.Nq + C::BQ * C::NQT - 1) / (C::BQ * C::NQT);
   p.total_units = p.BH * p.n_qb;
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.lse = a.lse;
   p.o = static_cast<__nv_bfloat16*>(a.o);
   p.o_sb = a.os[0];
   p.o_sh = a.os[1];
   p.o_sn = a.os[2];
-  p.lse = a.lse;
   p.status = ctx.status;
   p.limit_ns = ctx.limit_ns;
   const int grid = p.total_units < ctx.num_sms ? p.total_units : ctx.num_sms;
-  kernel<<<grid, C::THREADS, C::SMEM_ALLOC, ctx.stream>>>(mq, mk, mv, p);
+  kernel<<<grid, C::THREADS, C::SMEM_ALLOC, ctx.stream>>>(mq, mk, mv, mo, p);
   return static_cast<int>(cudaGetLastError());
 }
 
