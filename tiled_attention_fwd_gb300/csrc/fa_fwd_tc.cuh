@@ -388,14 +388,33 @@ struct TcMma {
     k_lo = sdesc_lo(base + C::OFF_KV, 16);
     v_lo = sdesc_lo(base + C::OFF_KV, C::KV_REGION);
   }
+  // Descriptor increments from K step k-1 to k.
+  struct QkSteps {
+    static constexpr __host__ __device__ uint32_t da(int k) { return q_step(k) - q_step(k - 1); }
+    static constexpr __host__ __device__ uint32_t db(int k) { return k_step(k) - k_step(k - 1); }
+  };
+  struct PvSteps {
+    static constexpr __host__ __device__ uint32_t ta(int) { return 8; }  // 16 bf16 = 8 TMEM columns
+    static constexpr __host__ __device__ uint32_t db(int) { return C::SWB; }
+  };
   // S[buf] = Q[qt] K^T with K at tile position kpos; completion on s_full_bar.
   __device__ __forceinline__ void qk(int qt, int buf, uint32_t kpos, uint32_t s_full_bar) const {
     const uint32_t d_t = tmem + C::TM_S + buf * C::TM_SB;
     const uint32_t a = q_lo + qt * QTILE_STEP;
     const uint32_t b = k_lo + kpos * TILE_STEP;
+    // d <= 128: one block per product (measured faster at d = 32 and 64, equal
+    // at d = 128); d = 256: one MMA per block (measured faster there).
+    if constexpr (D == 32) {
+      mma_ss_x2<QkSteps>(d_t, a, DESC_HI, b, DESC_HI, IDESC_QK, 0u);
+    } else if constexpr (D == 64) {
+      mma_ss_x4<QkSteps>(d_t, a, DESC_HI, b, DESC_HI, IDESC_QK, 0u);
+    } else if constexpr (D == 128) {
+      mma_ss_x8<QkSteps>(d_t, a, DESC_HI, b, DESC_HI, IDESC_QK, 0u);
+    } else {
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk)
-      mma_ss_elect(d_t, a + q_step(kk), DESC_HI, b + k_step(kk), DESC_HI, IDESC_QK, kk > 0 ? 1u : 0u);
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_ss_elect(d_t, a + q_step(kk), DESC_HI, b + k_step(kk), DESC_HI, IDESC_QK, kk > 0 ? 1u : 0u);
+    }
     commit(s_full_bar);
   }
   // O[ot] (+)= P[buf] V with V at tile position vpos.
@@ -403,9 +422,13 @@ struct TcMma {
     const uint32_t d_t = tmem + C::TM_O + ot * D;
     const uint32_t a_t = tmem + C::TM_S + buf * C::TM_SB;
     const uint32_t b = v_lo + vpos * TILE_STEP;
+    if constexpr (D <= 128) {
+      mma_ts_x8<PvSteps>(d_t, a_t, b, DESC_HI, IDESC_PV, acc ? 1u : 0u);
+    } else {
 #pragma unroll
-    for (int kk = 0; kk < C::BK / 16; ++kk)
-      mma_ts_elect(d_t, a_t + kk * 8, b + v_step(kk), DESC_HI, IDESC_PV, (acc || kk > 0) ? 1u : 0u);
+      for (int kk = 0; kk < C::BK / 16; ++kk)
+        mma_ts_elect(d_t, a_t + kk * 8, b + v_step(kk), DESC_HI, IDESC_PV, (acc || kk > 0) ? 1u : 0u);
+    }
   }
   __device__ __forceinline__ void commit(uint32_t bar) const { mma_commit_elect(bar); }
 };
