@@ -14,12 +14,13 @@
 //
 // Both kernels share one structure (template parameter MODE):
 //   MODE 0, dK/dV: a work unit is a 128-key tile of one head; its K and V
-//     tiles stay in shared memory while 64-row tiles of Q and dO stream past.
+//     tiles stay in shared memory while tiles of Q and dO (64 rows at d = 128,
+//     96 at d <= 64) stream past.
 //     S^T = K Q^T and dP^T = V dO^T go to TMEM (128 lanes = keys), the
 //     elementwise warps form P^T and dS^T in bf16 over them, and the MMA warp
 //     accumulates dV += P^T dO and dK += dS^T Q in TMEM.
 //   MODE 1, dQ: a work unit is a 128-row query tile; its Q and dO tiles stay,
-//     64-key tiles of K and V stream past; S = Q K^T, dP = dO V^T, then
+//     96-key tiles of K and V stream past; S = Q K^T, dP = dO V^T, then
 //     dQ += dS K.
 // Per CTA (one per SM, persistent): two elementwise warpgroups take the
 // streamed tiles alternately (S/dP double-buffered in TMEM), one MMA warp
@@ -267,29 +268,54 @@ struct BwdMma {
     b1_mn = sdesc_lo(base + C::OFF_ST, C::S_REGION);
     b2_mn = sdesc_lo(base + C::OFF_ST + C::S_TILE, C::S_REGION);
   }
+  // Descriptor increments from K step k-1 to k (16-byte units; TMEM columns for ta).
+  struct SdpSteps {
+    static constexpr __host__ __device__ uint32_t da(int k) { return a_step(k) - a_step(k - 1); }
+    static constexpr __host__ __device__ uint32_t db(int k) { return b_step(k) - b_step(k - 1); }
+  };
+  struct AccSteps {
+    static constexpr __host__ __device__ uint32_t ta(int) { return 8; }  // 16 bf16 = 8 TMEM columns
+    static constexpr __host__ __device__ uint32_t db(int k) { return mn_step(k) - mn_step(k - 1); }
+  };
+  // d >= 64 issues each product's MMAs as one run; d = 32 one MMA per block
+  // (measured faster there).
+  static constexpr bool RUNS = D >= 64;
   // S = A1 B1^T and dP = A2 B2^T of the tile in stage st, into buffer b.
   __device__ __forceinline__ void sdp(uint32_t st, int b) const {
     const uint32_t d_s = tmem + C::TM_S + b * C::BS, d_p = tmem + C::TM_DP + b * C::BS;
+    if constexpr (RUNS) {
+      mma_ss_run<D / 16, SdpSteps>(d_s, a1, DESC_HI, b1 + st * STAGE_STEP, DESC_HI, IDESC_S, 0u);
+      mma_ss_run<D / 16, SdpSteps>(d_p, a2, DESC_HI, b2 + st * STAGE_STEP, DESC_HI, IDESC_S, 0u);
+    } else {
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk)
-      mma_ss_elect(d_s, a1 + a_step(kk), DESC_HI, b1 + st * STAGE_STEP + b_step(kk), DESC_HI, IDESC_S, kk > 0);
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_ss_elect(d_s, a1 + a_step(kk), DESC_HI, b1 + st * STAGE_STEP + b_step(kk), DESC_HI, IDESC_S, kk > 0);
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk)
-      mma_ss_elect(d_p, a2 + a_step(kk), DESC_HI, b2 + st * STAGE_STEP + b_step(kk), DESC_HI, IDESC_S, kk > 0);
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_ss_elect(d_p, a2 + a_step(kk), DESC_HI, b2 + st * STAGE_STEP + b_step(kk), DESC_HI, IDESC_S, kk > 0);
+    }
   }
   // MODE 0: dK (+)= dS^T B1 and dV (+)= P^T B2.  MODE 1: dQ (+)= dS B1.
   // dS (bf16) sits over the dP buffer, P (bf16) over the S buffer.
   __device__ __forceinline__ void accumulate(uint32_t st, int b, bool acc) const {
     const uint32_t a_ds = tmem + C::TM_DP + b * C::BS, a_p = tmem + C::TM_S + b * C::BS;
-#pragma unroll
-    for (int kk = 0; kk < C::BS / 16; ++kk)
-      mma_ts_elect(tmem + C::TM_OUT, a_ds + kk * 8, b1_mn + st * STAGE_STEP + mn_step(kk), DESC_HI, IDESC_O,
-                   (acc || kk > 0) ? 1u : 0u);
-    if constexpr (C::KV) {
+    if constexpr (RUNS) {
+      mma_ts_run<C::BS / 16, AccSteps>(tmem + C::TM_OUT, a_ds, b1_mn + st * STAGE_STEP, DESC_HI, IDESC_O,
+                                       acc ? 1u : 0u);
+      if constexpr (C::KV)
+        mma_ts_run<C::BS / 16, AccSteps>(tmem + C::TM_OUT + D, a_p, b2_mn + st * STAGE_STEP, DESC_HI, IDESC_O,
+                                         acc ? 1u : 0u);
+    } else {
 #pragma unroll
       for (int kk = 0; kk < C::BS / 16; ++kk)
-        mma_ts_elect(tmem + C::TM_OUT + D, a_p + kk * 8, b2_mn + st * STAGE_STEP + mn_step(kk), DESC_HI, IDESC_O,
+        mma_ts_elect(tmem + C::TM_OUT, a_ds + kk * 8, b1_mn + st * STAGE_STEP + mn_step(kk), DESC_HI, IDESC_O,
                      (acc || kk > 0) ? 1u : 0u);
+      if constexpr (C::KV) {
+#pragma unroll
+        for (int kk = 0; kk < C::BS / 16; ++kk)
+          mma_ts_elect(tmem + C::TM_OUT + D, a_p + kk * 8, b2_mn + st * STAGE_STEP + mn_step(kk), DESC_HI,
+                       IDESC_O, (acc || kk > 0) ? 1u : 0u);
+      }
     }
   }
 };

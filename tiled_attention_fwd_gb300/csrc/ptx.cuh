@@ -269,7 +269,7 @@ __device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, u
       "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-// A run of n MMAs (n = 2, 4, 8) over consecutive 16-wide K steps, issued by
+// A run of n MMAs (n = 2, 4, 6, 8) over consecutive 16-wide K steps, issued by
 // one elected lane from a single block: the descriptors advance by the
 // compile-time increments S::da(k) / S::db(k) (16-byte units, step k-1 to k;
 // for the TMEM A operand S::ta(k) columns), and only the first MMA takes the
@@ -359,6 +359,66 @@ __device__ __forceinline__ void mma_ts_x4(uint32_t d_tmem, uint32_t a_tmem, uint
       : "memory");
 }
 template <class S>
+__device__ __forceinline__ void mma_ss_x6(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo, uint32_t b_hi,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred PE, PA, PT;\n\t.reg .b64 DA, DB;\n\t"
+      "setp.ne.b32 PA, %6, 0;\n\t"
+      "setp.eq.b32 PT, 0, 0;\n\t"
+      "mov.b64 DA, {%1, %2};\n\t"
+      "mov.b64 DB, {%3, %4};\n\t"
+      "elect.sync _|PE, 0xffffffff;\n\t"
+      "@PE tcgen05.mma.cta_group::1.kind::f16 [%0], DA, DB, %5, PA;\n\t"
+      "add.s64 DA, DA, %7;\n\t"
+      "add.s64 DB, DB, %12;\n\t"
+      "@PE tcgen05.mma.cta_group::1.kind::f16 [%0], DA, DB, %5, PT;\n\t"
+      "add.s64 DA, DA, %8;\n\t"
+      "add.s64 DB, DB, %13;\n\t"
+      "@PE tcgen05.mma.cta_group::1.kind::f16 [%0], DA, DB, %5, PT;\n\t"
+      "add.s64 DA, DA, %9;\n\t"
+      "add.s64 DB, DB, %14;\n\t"
+      "@PE tcgen05.mma.cta_group::1.kind::f16 [%0], DA, DB, %5, PT;\n\t"
+      "add.s64 DA, DA, %10;\n\t"
+      "add.s64 DB, DB, %15;\n\t"
+      "@PE tcgen05.mma.cta_group::1.kind::f16 [%0], DA, DB, %5, PT;\n\t"
+      "add.s64 DA, DA, %11;\n\t"
+      "add.s64 DB, DB, %16;\n\t"
+      "@PE tcgen05.mma.cta_group::1.kind::f16 [%0], DA, DB, %5, PT;\n\t"
+      "}"
+      ::"r"(d_tmem), "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate), "n"(S::da(1)), "n"(S::da(2)), "n"(S::da(3)), "n"(S::da(4)), "n"(S::da(5)), "n"(S::db(1)), "n"(S::db(2)), "n"(S::db(3)), "n"(S::db(4)), "n"(S::db(5))
+      : "memory");
+}
+template <class S>
+__device__ __forceinline__ void mma_ts_x6(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred PE, PA, PT;\n\t.reg .b64 DB;\n\t.reg .b32 TA;\n\t"
+      "setp.ne.b32 PA, %5, 0;\n\t"
+      "setp.eq.b32 PT, 0, 0;\n\t"
+      "mov.b32 TA, %1;\n\t"
+      "mov.b64 DB, {%2, %3};\n\t"
+      "elect.sync _|PE, 0xffffffff;\n\t"
+      "@PE tcgen05.mma.cta_group::1.kind::f16 [%0], [TA], DB, %4, PA;\n\t"
+      "add.u32 TA, TA, %6;\n\t"
+      "add.s64 DB, DB, %11;\n\t"
+      "@PE tcgen05.mma.cta_group::1.kind::f16 [%0], [TA], DB, %4, PT;\n\t"
+      "add.u32 TA, TA, %7;\n\t"
+      "add.s64 DB, DB, %12;\n\t"
+      "@PE tcgen05.mma.cta_group::1.kind::f16 [%0], [TA], DB, %4, PT;\n\t"
+      "add.u32 TA, TA, %8;\n\t"
+      "add.s64 DB, DB, %13;\n\t"
+      "@PE tcgen05.mma.cta_group::1.kind::f16 [%0], [TA], DB, %4, PT;\n\t"
+      "add.u32 TA, TA, %9;\n\t"
+      "add.s64 DB, DB, %14;\n\t"
+      "@PE tcgen05.mma.cta_group::1.kind::f16 [%0], [TA], DB, %4, PT;\n\t"
+      "add.u32 TA, TA, %10;\n\t"
+      "add.s64 DB, DB, %15;\n\t"
+      "@PE tcgen05.mma.cta_group::1.kind::f16 [%0], [TA], DB, %4, PT;\n\t"
+      "}"
+      ::"r"(d_tmem), "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate), "n"(S::ta(1)), "n"(S::ta(2)), "n"(S::ta(3)), "n"(S::ta(4)), "n"(S::ta(5)), "n"(S::db(1)), "n"(S::db(2)), "n"(S::db(3)), "n"(S::db(4)), "n"(S::db(5))
+      : "memory");
+}
+template <class S>
 __device__ __forceinline__ void mma_ss_x8(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo, uint32_t b_hi,
                                            uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -431,6 +491,25 @@ __device__ __forceinline__ void mma_ts_x8(uint32_t d_tmem, uint32_t a_tmem, uint
       : "memory");
 }
 
+// Runs of N = 2, 4, 6 or 8 MMAs.
+template <int N, class S>
+__device__ __forceinline__ void mma_ss_run(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo, uint32_t b_hi,
+                                           uint32_t idesc, uint32_t accumulate) {
+  static_assert(N == 2 || N == 4 || N == 6 || N == 8, "run length");
+  if constexpr (N == 2) mma_ss_x2<S>(d_tmem, a_lo, a_hi, b_lo, b_hi, idesc, accumulate);
+  if constexpr (N == 4) mma_ss_x4<S>(d_tmem, a_lo, a_hi, b_lo, b_hi, idesc, accumulate);
+  if constexpr (N == 6) mma_ss_x6<S>(d_tmem, a_lo, a_hi, b_lo, b_hi, idesc, accumulate);
+  if constexpr (N == 8) mma_ss_x8<S>(d_tmem, a_lo, a_hi, b_lo, b_hi, idesc, accumulate);
+}
+template <int N, class S>
+__device__ __forceinline__ void mma_ts_run(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                           uint32_t idesc, uint32_t accumulate) {
+  static_assert(N == 2 || N == 4 || N == 6 || N == 8, "run length");
+  if constexpr (N == 2) mma_ts_x2<S>(d_tmem, a_tmem, b_lo, b_hi, idesc, accumulate);
+  if constexpr (N == 4) mma_ts_x4<S>(d_tmem, a_tmem, b_lo, b_hi, idesc, accumulate);
+  if constexpr (N == 6) mma_ts_x6<S>(d_tmem, a_tmem, b_lo, b_hi, idesc, accumulate);
+  if constexpr (N == 8) mma_ts_x8<S>(d_tmem, a_tmem, b_lo, b_hi, idesc, accumulate);
+}
 
 // Arrive once on `bar` when every tcgen05 operation the warp issued so far
 // has completed (issued by one elected lane).
