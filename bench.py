@@ -399,8 +399,8 @@ def run_ours_bwd(args, w):
     import tiled_attention_fwd_gb300 as fa
     from tiled_attention_fwd_gb300.inputs import make_dout, make_qkv
 
-    if w.dtype != "bf16" or w.d not in (32, 64, 128):
-        raise SystemExit(f"the backward pass covers bf16 with d in (32, 64, 128), not {w.name}")
+    if w.dtype != "bf16" or w.d not in (32, 64, 128, 256):
+        raise SystemExit(f"the backward pass covers bf16 with d in (32, 64, 128, 256), not {w.name}")
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))

@@ -157,7 +157,9 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
  *                      o and lse are the outputs of fa_fwd for q, k, v, scale, causal.
  *   lse              : device pointer to fp32 [B][H][N].
  *   dq, dk, dv       : device pointers to bf16 [B][H][N][d], 16-byte aligned; fully overwritten.
- *   d                : head dimension, one of 32, 64, 128 (else FA_ERR_UNSUPPORTED_D).
+ *   d                : head dimension, one of 32, 64, 128, 256 (else FA_ERR_UNSUPPORTED_D);
+ *                      d = 256 runs 32-row streamed tiles and, for dK and dV, one output half
+ *                      per work unit (the TMEM of one SM holds no more).
  *   workspace        : device pointer, 256-byte aligned, at least fa_bwd_workspace_bytes(B, H, N, d)
  *                      bytes (else FA_ERR_WORKSPACE); its contents on entry are ignored.
  *   Other arguments and behaviour as fa_fwd.

@@ -22,6 +22,9 @@ SHAPES = [
     (2, 2, 257, 128),
     (1, 3, 1000, 128),
     (1, 2, 513, 32),
+    (1, 2, 200, 256),
+    (2, 1, 129, 256),
+    (1, 1, 1, 256),
 ]
 
 
@@ -71,11 +74,11 @@ def test_backward_is_deterministic():
 
 def test_backward_rejects_bad_arguments():
     dev = torch.device("cuda", 0)
-    x = torch.zeros((1, 1, 64, 256), device=dev, dtype=torch.bfloat16)
+    x = torch.zeros((1, 1, 64, 48), device=dev, dtype=torch.bfloat16)
     lse = torch.zeros((1, 1, 64), device=dev, dtype=torch.float32)
     with pytest.raises(FAError) as e:
         backward(x, x, x, x, lse, x)
-    assert e.value.code == -3  # FA_ERR_UNSUPPORTED_D: d = 256 has no backward kernel
+    assert e.value.code == -3  # FA_ERR_UNSUPPORTED_D: no kernel for d = 48
     y = torch.zeros((1, 1, 64, 64), device=dev, dtype=torch.bfloat16)
     lse = torch.zeros((1, 1, 64), device=dev, dtype=torch.float32)
     small = torch.empty(fa_bwd_workspace_bytes(1, 1, 64, 64) - 256, device=dev, dtype=torch.uint8)

@@ -44,6 +44,8 @@ def _fwd_bwd(q, k, v, do, causal, scale, o_out=None, grads_out=None):
     (2, 2, 1, 257, 128),
     (1, 3, 513, 1, 128),
     (1, 1, 200, 70, 32),
+    (1, 2, 100, 300, 256),   # d = 256: causal key units past the last query, both output halves
+    (1, 1, 300, 97, 256),
 ])
 def test_rectangular_matches_oracle(B, H, Nq, Nk, d, causal):
     dev = torch.device("cuda", 0)
@@ -60,7 +62,7 @@ def test_rectangular_matches_oracle(B, H, Nq, Nk, d, causal):
 
 
 @pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
-@pytest.mark.parametrize("d", [32, 64, 128])
+@pytest.mark.parametrize("d", [32, 64, 128, 256])
 def test_bshd_layout_matches_oracle(d, causal):
     """All eight tensors stored as [B, N, H, d] and passed as [B, H, N, d] views."""
     dev = torch.device("cuda", 0)

@@ -130,7 +130,7 @@ def test_backward_workspace_size_and_host_checks(lib):
     assert fa.fa_bwd(*ptrs, *common, FAKE + 16, n, None) == -4         # workspace not 256-byte aligned
     assert fa.fa_bwd(*ptrs, *common, 0, n, None) == -1                 # workspace missing
     assert fa.fa_bwd(*ptrs[:5], 0, *ptrs[6:], *common, ws, n, None) == -1   # dO missing
-    assert fa.fa_bwd(*ptrs, 2, 3, 100, 256, 0.125, 0, ws, n, None) == -3    # no d = 256 backward
+    assert fa.fa_bwd(*ptrs, 2, 3, 100, 48, 0.125, 0, ws, n, None) == -3     # no d = 48 kernel
     assert fa.fa_bwd(*ptrs, 2, 3, 100, 64, -1.0, 0, ws, n, None) == -8
     bad = list(ptrs)
     bad[6] = FAKE + 8
@@ -140,11 +140,11 @@ def test_backward_workspace_size_and_host_checks(lib):
 def test_backward_kernels_do_not_spill():
     if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
         pytest.skip("nvcc not available")
-    rep = build.ptxas_report({f"fa_bwd_d{d}{s}.cu" for d in (32, 64, 128) for s in ("", "_strided")})
+    rep = build.ptxas_report({f"fa_bwd_d{d}{s}.cu" for d in (32, 64, 128, 256) for s in ("", "_strided")})
     ks = {k: v for k, v in rep.items() if "fa_bwd" in k}
     # per head dimension: 8 tensor-core kernels (dK/dV or dQ x causal or not x contiguous or
     # strided) and 1 preprocessing kernel
-    assert len(ks) == 27
+    assert len(ks) == 36
     for name, r in ks.items():
         assert r["spill_stores"] == 0 and r["spill_loads"] == 0, (name, r)
 
@@ -177,7 +177,7 @@ def test_strided_backward_rejects_bad_arguments_on_host(lib):
     assert call(strides=st[:5] + [(1 << 20, 1 << 14, 132)] + st[6:]) == -4   # dq row stride not 16-byte
     assert call(strides=st[:6] + [(0, 8, 8)] + st[7:]) == -2          # dk batch stride 0
     assert call(Nk=0) == -2
-    assert call(d=256) == -3
+    assert call(d=48) == -3
     assert call(scale=float("nan")) == -8
     assert call(ptrs=ptrs[:8] + [0]) == -1                            # dv missing
     assert call(ptrs=ptrs[:2] + [FAKE + 4] + ptrs[3:]) == -4          # v not 16-byte aligned

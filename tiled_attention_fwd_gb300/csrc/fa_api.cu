@@ -391,7 +391,8 @@ int run_bwd(BwdArgs& a, int d, bool strided, void* workspace, size_t workspace_b
   switch (d) {
     case 32: e = strided ? launch_bwd_strided_d32(a, ctx) : launch_bwd_d32(a, ctx); break;
     case 64: e = strided ? launch_bwd_strided_d64(a, ctx) : launch_bwd_d64(a, ctx); break;
-    default: e = strided ? launch_bwd_strided_d128(a, ctx) : launch_bwd_d128(a, ctx); break;
+    case 128: e = strided ? launch_bwd_strided_d128(a, ctx) : launch_bwd_d128(a, ctx); break;
+    default: e = strided ? launch_bwd_strided_d256(a, ctx) : launch_bwd_d256(a, ctx); break;
   }
   return e == 0 ? FA_OK : FA_ERR_CUDA;
 }
@@ -404,7 +405,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
            size_t workspace_bytes, void* stream) {
   int rc = fa::check_common(B, H, N, d, scale);
   if (rc != FA_OK) return rc;
-  if (d != 32 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED_D;
+  if (d != 32 && d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED_D;
   fa::BwdArgs a;
   a.q = q;
   a.k = k;
@@ -433,7 +434,7 @@ int fa_bwd_strided(const void* q, const void* k, const void* v, const void* o, c
   if (rc != FA_OK) return rc;
   rc = fa::check_common(B, H, Nk, d, scale);
   if (rc != FA_OK) return rc;
-  if (d != 32 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED_D;
+  if (d != 32 && d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED_D;
   for (int i = 0; i < 24; ++i)
     if (strides[i] < 1 || strides[i] >= (1LL << 38)) return FA_ERR_BAD_SHAPE;
   for (int i = 0; i < 24; ++i)

@@ -38,7 +38,7 @@ int launch_bwd_main(const BwdArgs& a, const LaunchCtx& ctx) {
   p.n_pad = a.n_pad;
   p.n_m = (n_fix + C::BM - 1) / C::BM;
   p.n_s = (n_str + C::BS - 1) / C::BS;
-  p.total_units = p.BH * p.n_m;
+  p.total_units = p.BH * p.n_m * C::HALVES;
   p.scale = a.scale;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.l2 = a.l2;

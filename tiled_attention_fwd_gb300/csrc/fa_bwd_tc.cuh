@@ -42,7 +42,7 @@ struct BwdParams {
   int n_pad;             // row stride of the l2 / dsum vectors: N rounded up to 192 (a multiple of every BS)
   int n_m;               // 128-row tiles of the fixed operands per head: ceil(N / 128)
   int n_s;               // streamed tiles per head: ceil(N / BS)
-  int total_units;       // BH * n_m
+  int total_units;       // BH * n_m * HALVES
   float scale;           // softmax scale (dK and dQ carry one factor of it)
   float scale_log2;      // scale * log2(e)
   const float* l2;       // [BH][n_pad]: L * log2(e); +inf on rows >= N
@@ -63,7 +63,13 @@ struct BwdCfg {
   // the accumulators (4 * 96 + D in MODE 1; 4 * 96 + 2 * D in MODE 0 for
   // d <= 64), else 64 (MODE 0 at d = 128: 4 * 64 + 2 * 128 = 512 columns).
   // Larger tiles mean fewer, larger S and dP products per FLOP for the MMA warp.
-  static constexpr int BS = (KV && D == 128) ? 64 : 96;
+  // d = 256: 32 rows (two 128-row fixed tiles of 64 KB each leave room for
+  // two or three stages of 32-row tiles), and in MODE 0 each unit accumulates
+  // one half of the dK and dV columns (HALVES units per key tile), so that
+  // 4 * 32 + 2 * 128 columns of TMEM suffice.
+  static constexpr int BS = (D == 256) ? 32 : (KV && D == 128) ? 64 : 96;
+  static constexpr int HALVES = (KV && D == 256) ? 2 : 1;
+  static constexpr int OUTW = D / HALVES;                // accumulator columns per output
   static constexpr int SWB = (D * 2 >= 128) ? 128 : D * 2;  // swizzle span in bytes
   static constexpr uint32_t SWZ = (SWB == 128) ? 2u : 4u;   // descriptor swizzle code
   static constexpr int RC = SWB / 2;                     // bf16 columns per swizzle region
@@ -94,22 +100,27 @@ struct BwdCfg {
   static constexpr int TM_OUT = 4 * BS;
   static constexpr int NOUT = KV ? 2 : 1;
   static constexpr int TM_COLS = 512;
+  // S and dP issued as runs of MMAs from one block (d >= 64; d = 256 as two
+  // runs of 8), or one MMA per block (d = 32, measured faster there).
+  static constexpr bool RUNS = D >= 64;
   // Warps: 0-3 and 4-7 elementwise warpgroups (buffer 0 / 1), 8 MMA, 9 TMA.
   static constexpr int MMA_WARP = 8;
   static constexpr int LOAD_WARP = 9;
   static constexpr int THREADS = 320;
-  static_assert(D == 32 || D == 64 || D == 128, "head dim of the backward pass");
-  static_assert(TM_OUT + NOUT * D <= TM_COLS, "TMEM budget");
+  static_assert(D == 32 || D == 64 || D == 128 || D == 256, "head dim of the backward pass");
+  static_assert(TM_OUT + NOUT * OUTW <= TM_COLS, "TMEM budget");
   static_assert(NST >= 2, "streamed stages");
   static_assert(SMEM_USED <= SMEM_LIMIT, "shared memory budget");
 };
 
-// A work unit: fixed rows [m0, m0 + 128) of head bh, streamed tiles [s_begin, s_end).
+// A work unit: fixed rows [m0, m0 + 128) of head bh, streamed tiles
+// [s_begin, s_end), output columns [half * OUTW, (half + 1) * OUTW).
 struct BwdUnit {
   int bh;
   int m0;
   int s_begin;
   int s_end;
+  int half;
 };
 
 // Units are numbered heaviest first under the causal mask: in MODE 0 the
@@ -118,8 +129,11 @@ struct BwdUnit {
 // of the diagonal are skipped.
 template <int D, int MODE, bool CAUSAL>
 __device__ __forceinline__ BwdUnit bwd_decode(int u, const BwdParams& p) {
+  constexpr int HV = BwdCfg<D, MODE>::HALVES;
   BwdUnit w;
-  const int mt = (MODE == 0) ? (u / p.BH) : (p.n_m - 1 - u / p.BH);
+  const int per_tile = p.BH * HV;  // units per fixed tile
+  const int mt = (MODE == 0) ? (u / per_tile) : (p.n_m - 1 - u / per_tile);
+  w.half = (u % per_tile) / p.BH;
   w.bh = u % p.BH;
   w.m0 = mt * 128;
   if (MODE == 0) {
@@ -244,7 +258,7 @@ template <int D, int MODE>
 struct BwdMma {
   using C = BwdCfg<D, MODE>;
   static constexpr uint32_t IDESC_S = make_idesc_bf16(128, C::BS, 0);  // S, dP: B K-major
-  static constexpr uint32_t IDESC_O = make_idesc_bf16(128, D, 1);      // accumulators: B MN-major
+  static constexpr uint32_t IDESC_O = make_idesc_bf16(128, C::OUTW, 1);  // accumulators: B MN-major
   static constexpr uint32_t DESC_HI = sdesc_hi(8 * C::SWB, C::SWZ);
   static constexpr __host__ __device__ uint32_t a_step(int kk) {
     return ((kk * 16 / C::RC) * C::FIX_REGION + (kk * 16 % C::RC) * 2) >> 4;
@@ -269,23 +283,30 @@ struct BwdMma {
     b2_mn = sdesc_lo(base + C::OFF_ST + C::S_TILE, C::S_REGION);
   }
   // Descriptor increments from K step k-1 to k (16-byte units; TMEM columns for ta).
+  template <int OFF>  // runs that start at K step OFF
   struct SdpSteps {
-    static constexpr __host__ __device__ uint32_t da(int k) { return a_step(k) - a_step(k - 1); }
-    static constexpr __host__ __device__ uint32_t db(int k) { return b_step(k) - b_step(k - 1); }
+    static constexpr __host__ __device__ uint32_t da(int k) { return a_step(OFF + k) - a_step(OFF + k - 1); }
+    static constexpr __host__ __device__ uint32_t db(int k) { return b_step(OFF + k) - b_step(OFF + k - 1); }
   };
   struct AccSteps {
     static constexpr __host__ __device__ uint32_t ta(int) { return 8; }  // 16 bf16 = 8 TMEM columns
     static constexpr __host__ __device__ uint32_t db(int k) { return mn_step(k) - mn_step(k - 1); }
   };
-  // d >= 64 issues each product's MMAs as one run; d = 32 one MMA per block
-  // (measured faster there).
-  static constexpr bool RUNS = D >= 64;
+  static constexpr bool RUNS = C::RUNS;
+  // Start of output half h within a streamed tile read MN-major: OUTW / 64 regions per half.
+  static constexpr uint32_t HALF_STEP = (C::OUTW / C::RC) * C::S_REGION >> 4;
   // S = A1 B1^T and dP = A2 B2^T of the tile in stage st, into buffer b.
   __device__ __forceinline__ void sdp(uint32_t st, int b) const {
     const uint32_t d_s = tmem + C::TM_S + b * C::BS, d_p = tmem + C::TM_DP + b * C::BS;
-    if constexpr (RUNS) {
-      mma_ss_run<D / 16, SdpSteps>(d_s, a1, DESC_HI, b1 + st * STAGE_STEP, DESC_HI, IDESC_S, 0u);
-      mma_ss_run<D / 16, SdpSteps>(d_p, a2, DESC_HI, b2 + st * STAGE_STEP, DESC_HI, IDESC_S, 0u);
+    if constexpr (RUNS && D <= 128) {
+      mma_ss_run<D / 16, SdpSteps<0>>(d_s, a1, DESC_HI, b1 + st * STAGE_STEP, DESC_HI, IDESC_S, 0u);
+      mma_ss_run<D / 16, SdpSteps<0>>(d_p, a2, DESC_HI, b2 + st * STAGE_STEP, DESC_HI, IDESC_S, 0u);
+    } else if constexpr (RUNS) {
+      const uint32_t bs = b1 + st * STAGE_STEP, bp = b2 + st * STAGE_STEP;
+      mma_ss_run<8, SdpSteps<0>>(d_s, a1, DESC_HI, bs, DESC_HI, IDESC_S, 0u);
+      mma_ss_run<8, SdpSteps<8>>(d_s, a1 + a_step(8), DESC_HI, bs + b_step(8), DESC_HI, IDESC_S, 1u);
+      mma_ss_run<8, SdpSteps<0>>(d_p, a2, DESC_HI, bp, DESC_HI, IDESC_S, 0u);
+      mma_ss_run<8, SdpSteps<8>>(d_p, a2 + a_step(8), DESC_HI, bp + b_step(8), DESC_HI, IDESC_S, 1u);
     } else {
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
@@ -296,25 +317,27 @@ struct BwdMma {
     }
   }
   // MODE 0: dK (+)= dS^T B1 and dV (+)= P^T B2.  MODE 1: dQ (+)= dS B1.
-  // dS (bf16) sits over the dP buffer, P (bf16) over the S buffer.
-  __device__ __forceinline__ void accumulate(uint32_t st, int b, bool acc) const {
+  // dS (bf16) sits over the dP buffer, P (bf16) over the S buffer.  Output
+  // half h takes B's columns [h * OUTW, (h + 1) * OUTW).
+  __device__ __forceinline__ void accumulate(uint32_t st, int b, bool acc, int half) const {
     const uint32_t a_ds = tmem + C::TM_DP + b * C::BS, a_p = tmem + C::TM_S + b * C::BS;
+    const uint32_t hs = static_cast<uint32_t>(half) * HALF_STEP;
     if constexpr (RUNS) {
-      mma_ts_run<C::BS / 16, AccSteps>(tmem + C::TM_OUT, a_ds, b1_mn + st * STAGE_STEP, DESC_HI, IDESC_O,
+      mma_ts_run<C::BS / 16, AccSteps>(tmem + C::TM_OUT, a_ds, b1_mn + st * STAGE_STEP + hs, DESC_HI, IDESC_O,
                                        acc ? 1u : 0u);
       if constexpr (C::KV)
-        mma_ts_run<C::BS / 16, AccSteps>(tmem + C::TM_OUT + D, a_p, b2_mn + st * STAGE_STEP, DESC_HI, IDESC_O,
-                                         acc ? 1u : 0u);
+        mma_ts_run<C::BS / 16, AccSteps>(tmem + C::TM_OUT + C::OUTW, a_p, b2_mn + st * STAGE_STEP + hs, DESC_HI,
+                                         IDESC_O, acc ? 1u : 0u);
     } else {
 #pragma unroll
       for (int kk = 0; kk < C::BS / 16; ++kk)
-        mma_ts_elect(tmem + C::TM_OUT, a_ds + kk * 8, b1_mn + st * STAGE_STEP + mn_step(kk), DESC_HI, IDESC_O,
-                     (acc || kk > 0) ? 1u : 0u);
+        mma_ts_elect(tmem + C::TM_OUT, a_ds + kk * 8, b1_mn + st * STAGE_STEP + hs + mn_step(kk), DESC_HI,
+                     IDESC_O, (acc || kk > 0) ? 1u : 0u);
       if constexpr (C::KV) {
 #pragma unroll
         for (int kk = 0; kk < C::BS / 16; ++kk)
-          mma_ts_elect(tmem + C::TM_OUT + D, a_p + kk * 8, b2_mn + st * STAGE_STEP + mn_step(kk), DESC_HI,
-                       IDESC_O, (acc || kk > 0) ? 1u : 0u);
+          mma_ts_elect(tmem + C::TM_OUT + C::OUTW, a_p + kk * 8, b2_mn + st * STAGE_STEP + hs + mn_step(kk),
+                       DESC_HI, IDESC_O, (acc || kk > 0) ? 1u : 0u);
       }
     }
   }
@@ -378,7 +401,7 @@ __device__ __forceinline__ void bwd_mma(const BwdParams& p, const BwdBars<D, MOD
         if (!(ok = wait(bar.out_free(), (uk - 1) & 1))) break;
         tc_fence_after();
       }
-      M.accumulate(stage_of(t), b, t > 0);
+      M.accumulate(stage_of(t), b, t > 0, w.half);
       mma_commit_elect(bar.st_empty(stage_of(t)));
       if (t + 2 < n) {
         if (!(ok = acquire(t + 2))) break;
@@ -503,7 +526,7 @@ __device__ __forceinline__ void bwd_elementwise(const BwdParams& p, const BwdBar
     if (!ok) break;
     tc_fence_after();
     const bool second = C::KV && b == 1;
-    const uint32_t acc = tmem + lane_off + C::TM_OUT + (second ? D : 0);
+    const uint32_t acc = tmem + lane_off + C::TM_OUT + (second ? C::OUTW : 0);
     __nv_bfloat16* out = second ? p.out1 : p.out0;
     const float f = second ? 1.f : p.scale;  // dK and dQ carry the softmax scale
     const uint64_t f2 = f2_pack(f, f);
@@ -517,7 +540,7 @@ __device__ __forceinline__ void bwd_elementwise(const BwdParams& p, const BwdBar
     }
     const bool empty = n <= 0;  // no streamed tile reached these rows: the gradients are zero
 #pragma unroll 1
-    for (int c = 0; c < D / 32; ++c) {
+    for (int c = 0; c < C::OUTW / 32; ++c) {
       if (!C::KV && (c & 1) != b) continue;
       uint32_t v[32];
       tmem_ld32(acc + c * 32, v);
@@ -533,7 +556,7 @@ __device__ __forceinline__ void bwd_elementwise(const BwdParams& p, const BwdBar
         packed[i] = pack_bf16x2(y.x, y.y);
       }
       if (row < n_rows) {
-        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+        uint4* dst = reinterpret_cast<uint4*>(orow + w.half * C::OUTW + c * 32);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
           dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);

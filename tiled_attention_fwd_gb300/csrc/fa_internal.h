@@ -111,10 +111,12 @@ struct BwdArgs {
 int launch_bwd_d32(const BwdArgs& a, const LaunchCtx& ctx);
 int launch_bwd_d64(const BwdArgs& a, const LaunchCtx& ctx);
 int launch_bwd_d128(const BwdArgs& a, const LaunchCtx& ctx);
+int launch_bwd_d256(const BwdArgs& a, const LaunchCtx& ctx);
 // The same for strided tensors (4-D tensor maps).  Defined in fa_bwd_d<D>_strided.cu.
 int launch_bwd_strided_d32(const BwdArgs& a, const LaunchCtx& ctx);
 int launch_bwd_strided_d64(const BwdArgs& a, const LaunchCtx& ctx);
 int launch_bwd_strided_d128(const BwdArgs& a, const LaunchCtx& ctx);
+int launch_bwd_strided_d256(const BwdArgs& a, const LaunchCtx& ctx);
 
 // The bf16 forward for d in {32, 64, 128, 256}; takes the contiguous kernels
 // when every tensor is contiguous [B][H][N][d], else the strided ones; returns
