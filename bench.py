@@ -534,6 +534,86 @@ def run_ours_bwd(args, w):
     return 0
 
 
+# ------------------------------------------------------------------ per-config report
+REPORT_WORKLOADS = [
+    "f32_b1h1n128d16", "f32_b1h1n128d16_causal", "bf16_b8h1n1024d64", "bf16_b8h1n1024d64_causal",
+    "bf16_b4h16n4096d128_causal", "bf16_b1h32n16384d128_causal", "bf16_b2h16n8192d32_qk3",
+    "bf16_b2h16n8192d64_qk3", "bf16_b2h16n8192d128_qk3", "bf16_b2h16n8192d256_qk3",
+]
+
+
+def run_report(args):
+    """Every config once: the forward's CUDA-event time over >= 20 launches (L2
+    flushed before each; median, min, max), its TFLOP/s and fraction of the
+    dense bf16 peak, beside the fp64 oracle timed in the same run on the host
+    cores (whole heads for about --report-cpu-seconds each; heads cost the same,
+    so the full config's oracle time is that rate scaled to all heads)."""
+    import torch
+
+    from tiled_attention_fwd_gb300 import check_status, fa_fwd, fa_fwd_f32
+    from tiled_attention_fwd_gb300.inputs import WORKLOADS, make_qkv
+
+    cores = os.cpu_count() or 1
+    pool = make_pool(cores)  # spawned before the first GPU call
+    peaks, peak_src = load_peaks()
+    peak = peaks["bf16_tflops"]
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    runs = max(20, args.steps)
+    rows = []
+    for name in REPORT_WORKLOADS:
+        w = WORKLOADS[name]
+        host = make_qkv(w)
+        q, k, v = (t.to(dev) for t in host)
+        o = torch.empty_like(q)
+        lse = torch.empty(q.shape[:-1], device=dev, dtype=torch.float32)
+
+        fn = fa_fwd if w.dtype == "bf16" else fa_fwd_f32
+        call = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), w.B, w.H, w.N, w.d,
+                float(w.scale), int(w.causal), torch.cuda.current_stream(dev).cuda_stream)
+
+        def launch():  # the C ABI directly, so that no host work sits between the events
+            rc = fn(*call)
+            if rc != 0:
+                raise RuntimeError(f"{fn.__name__} returned {rc}")
+
+        for _ in range(max(3, args.warmup)):
+            flush.zero_()
+            launch()
+        check_status(dev)
+        times = []
+        for _ in range(runs):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            launch()
+            b.record()
+            b.synchronize()
+            times.append(a.elapsed_time(b))
+        check_status(dev)
+        med = statistics.median(times)
+        tflops = w.flops / (med * 1e-3) / 1e12
+        ora, heads, secs = oracle_sample(w, args.report_cpu_seconds, pool, cores, host)
+        row = {"workload": name, "dtype": w.dtype, "causal": w.causal, "gflop": w.flops / 1e9,
+               "gpu_ms_median": med, "gpu_ms_min": min(times), "gpu_ms_max": max(times), "runs": runs,
+               "tflops": tflops, "frac_of_bf16_peak": tflops / peak, "peak_tflops": peak, "peak_source": peak_src,
+               "oracle_tflops": ora, "oracle_heads": heads, "oracle_s": secs,
+               "oracle_full_s": w.flops / (ora * 1e12), "oracle_cores": cores}
+        rows.append(row)
+        print(json.dumps(row), flush=True)
+    pool.close()
+    print(f"\n| config | GFLOP | GPU median / min / max (ms, {runs} runs) | TFLOP/s | of bf16 peak | "
+          f"CPU oracle ({cores} cores): TFLOP/s | oracle s, full config |")
+    print("|---|---|---|---|---|---|---|")
+    for r in rows:
+        print(f"| `{r['workload']}` | {r['gflop']:.3g} | {r['gpu_ms_median']:.4f} / {r['gpu_ms_min']:.4f} / "
+              f"{r['gpu_ms_max']:.4f} | {r['tflops']:.4g} | {r['frac_of_bf16_peak']:.3g} | "
+              f"{r['oracle_tflops']:.3g} | {r['oracle_full_s']:.3g} |")
+    return 0
+
+
 def main(argv=None):
     from tiled_attention_fwd_gb300.inputs import HEADLINE, WORKLOADS
 
@@ -548,7 +628,12 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU oracle sample budget")
     ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
                     help="forward pass (the headline) or backward pass (fa_bwd)")
+    ap.add_argument("--report", action="store_true",
+                    help="time the forward on every config beside the CPU oracle and print a table")
+    ap.add_argument("--report-cpu-seconds", type=float, default=8.0, help="CPU oracle budget per config in --report")
     args = ap.parse_args(argv)
+    if args.report:
+        return run_report(args)
     if args.impl == "ours":
         args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     w = WORKLOADS[args.workload]
