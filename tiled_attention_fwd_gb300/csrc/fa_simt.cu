@@ -6,8 +6,9 @@
 // lets every thread run the online-softmax recurrence for its own query.
 // Here a block of 4 warps owns 16 query rows (4 per warp) and stages 32 keys
 // per tile; within a warp, lane j scores key j of the tile against the row
-// (so the row max and sum are warp shuffles), and lane c accumulates output
-// columns c, c+32, ... of the row.  State (m, l, O) is fp32, as in the
+// (so the row max and sum are warp shuffles), the probabilities go through
+// shared memory, and lane c accumulates output columns c, c+32, ... of the
+// warp's rows (each V element read once for all of them).  State (m, l, O) is fp32, as in the
 // FlashAttention-2 forward of "FlashAttention-2 from PyTorch to Triton".
 #include <cmath>
 
@@ -44,6 +45,7 @@ __global__ void __launch_bounds__(kSimtWarps * 32)
   float* qs = sm;                            // [kSimtRows][d]
   float* kt = qs + kSimtRows * d;            // [kSimtKeys][ks]
   float* vt = kt + kSimtKeys * ks;           // [kSimtKeys][d]
+  float* pw = vt + kSimtKeys * d;            // [kSimtRows][kSimtKeys]: probabilities of the current tile
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
@@ -77,36 +79,54 @@ __global__ void __launch_bounds__(kSimtWarps * 32)
       vt[i] = in ? v[(head + key) * d + c] : 0.f;
     }
     __syncthreads();
+    // Scores and softmax statistics of the warp's rows (lane = key of the
+    // tile); each row's probabilities go to the warp's slice of pw.
     const int key = t0 + lane;
+    float alpha[kRowsPerWarp];
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i) {
       const int rl = warp * kRowsPerWarp + i;
       const int row = row_base + rl;
       const float* qr = qs + rl * d;
       const float* kr = kt + lane * ks;
-      float sc = 0.f;
-      for (int c = 0; c < d; ++c) sc = fmaf(qr[c], kr[c], sc);
-      sc *= scale;
+      float s0 = 0.f, s1 = 0.f;  // two partial sums for a shorter dependency chain
+      int c = 0;
+      for (; c + 1 < d; c += 2) {
+        s0 = fmaf(qr[c], kr[c], s0);
+        s1 = fmaf(qr[c + 1], kr[c + 1], s1);
+      }
+      if (c < d) s0 = fmaf(qr[c], kr[c], s0);
+      float sc = (s0 + s1) * scale;
       const bool valid = key < N && (!CAUSAL || key <= row);
       sc = valid ? sc : -INFINITY;
       const float m_new = fmaxf(m[i], warp_max(sc));
       const float base = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = expf(m[i] - base);  // 0 on the first tile (m = -inf)
-      const float pj = expf(sc - base);       // 0 for masked keys
-      l[i] = l[i] * alpha + warp_sum(pj);
-#pragma unroll
-      for (int t = 0; t < DPL; ++t) acc[i][t] *= alpha;
-      for (int j = 0; j < kSimtKeys; ++j) {
-        const float pjj = __shfl_sync(0xffffffffu, pj, j);
-        const float* vr = vt + j * d;
-#pragma unroll
-        for (int t = 0; t < DPL; ++t) {
-          const int c = lane + 32 * t;
-          if (c < d) acc[i][t] = fmaf(pjj, vr[c], acc[i][t]);
-        }
-      }
+      alpha[i] = expf(m[i] - base);  // 0 on the first tile (m = -inf)
+      const float pj = expf(sc - base);  // 0 for masked keys
+      l[i] = l[i] * alpha[i] + warp_sum(pj);
+      pw[(warp * kRowsPerWarp + i) * kSimtKeys + lane] = pj;
       m[i] = m_new;
     }
+    __syncwarp();
+    // O += P V: each V element is read once for the warp's rows; the
+    // probabilities are shared-memory broadcasts.
+#pragma unroll
+    for (int i = 0; i < kRowsPerWarp; ++i)
+#pragma unroll
+      for (int t = 0; t < DPL; ++t) acc[i][t] *= alpha[i];
+    const float* pr = pw + warp * kRowsPerWarp * kSimtKeys;
+#pragma unroll 4
+    for (int j = 0; j < kSimtKeys; ++j) {
+      const float* vr = vt + j * d;
+#pragma unroll
+      for (int t = 0; t < DPL; ++t) {
+        const int c = lane + 32 * t;
+        const float vv = c < d ? vr[c] : 0.f;
+#pragma unroll
+        for (int i = 0; i < kRowsPerWarp; ++i) acc[i][t] = fmaf(pr[i * kSimtKeys + j], vv, acc[i][t]);
+      }
+    }
+    __syncwarp();  // pw is rewritten by the next tile
   }
 
 #pragma unroll
@@ -127,7 +147,8 @@ template <int DPL, bool CAUSAL>
 int launch_simt_impl(const float* q, const float* k, const float* v, float* o, float* lse, int BH, int N, int d,
                      float scale, const LaunchCtx& ctx) {
   const size_t smem = sizeof(float) * (static_cast<size_t>(kSimtRows) * d + static_cast<size_t>(kSimtKeys) * (d | 1) +
-                                       static_cast<size_t>(kSimtKeys) * d);
+                                       static_cast<size_t>(kSimtKeys) * d +
+                                       static_cast<size_t>(kSimtRows) * kSimtKeys);
   auto kernel = fa_fwd_simt_kernel<DPL, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return static_cast<int>(e);
