@@ -143,6 +143,114 @@ __global__ void __launch_bounds__(kSimtWarps * 32)
   }
 }
 
+// Whole-head variant for small problems (the fp32 workload has N = 128,
+// d = 16).  K and V of the block's head are staged in shared memory once,
+// each warp owns one query row, and the row's scores against all keys are
+// formed before any exponential (lane j takes keys j, j + 32, ...), so the
+// softmax is the plain two-pass one: row max, then exponentials and their
+// sum; O is accumulated from the probabilities of all keys at once.  The
+// tiled kernel above reloads K/V per tile and serialises one global-memory
+// round trip, two block barriers and the online rescale per 32 keys, which at
+// this size costs more than the arithmetic.
+constexpr int kSmallWarps = 4;  // rows per block
+
+size_t small_smem_bytes(int N, int d) {
+  return sizeof(float) * (static_cast<size_t>(N) * (d | 1) + static_cast<size_t>(N) * d +
+                          static_cast<size_t>(kSmallWarps) * N + static_cast<size_t>(kSmallWarps) * d);
+}
+
+template <int DPL, bool CAUSAL>
+__global__ void __launch_bounds__(kSmallWarps * 32)
+    fa_fwd_simt_small_kernel(const float* __restrict__ q, const float* __restrict__ k, const float* __restrict__ v,
+                             float* __restrict__ o, float* __restrict__ lse, int N, int d, float scale) {
+  extern __shared__ float sm[];
+  const int ks = d | 1;  // odd row stride: lane-strided reads of K hit distinct banks
+  float* kt = sm;                                  // [N][ks]
+  float* vt = kt + static_cast<size_t>(N) * ks;    // [N][d]
+  float* pw = vt + static_cast<size_t>(N) * d;     // [kSmallWarps][N]: the row's scores, then probabilities
+  float* qw = pw + kSmallWarps * N;                // [kSmallWarps][d]: the row of Q
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const size_t head = static_cast<size_t>(blockIdx.y) * N;
+  const int row = blockIdx.x * kSmallWarps + warp;
+
+  const float* kh = k + head * d;
+  const float* vh = v + head * d;
+  for (int i = tid; i < N * d; i += blockDim.x) {
+    const int j = i / d, c = i - j * d;
+    kt[j * ks + c] = kh[i];
+    vt[i] = vh[i];
+  }
+  float* qr = qw + warp * d;
+  if (row < N)
+    for (int c = lane; c < d; c += 32) qr[c] = q[(head + row) * d + c];
+  __syncthreads();
+  if (row >= N) return;
+
+  const int kend = CAUSAL ? row + 1 : N;  // keys this row sees
+  float* pr = pw + warp * N;
+  // Scores, and the row max.
+  float mx = -INFINITY;
+  for (int key = lane; key < kend; key += 32) {
+    const float* kr = kt + key * ks;
+    float s0 = 0.f, s1 = 0.f;
+    int c = 0;
+    for (; c + 1 < d; c += 2) {
+      s0 = fmaf(qr[c], kr[c], s0);
+      s1 = fmaf(qr[c + 1], kr[c + 1], s1);
+    }
+    if (c < d) s0 = fmaf(qr[c], kr[c], s0);
+    const float sc = (s0 + s1) * scale;
+    pr[key] = sc;
+    mx = fmaxf(mx, sc);
+  }
+  mx = warp_max(mx);
+  // Probabilities and their sum (every row sees key 0, so mx is finite).
+  float sum = 0.f;
+  for (int key = lane; key < kend; key += 32) {
+    const float p = expf(pr[key] - mx);
+    pr[key] = p;
+    sum += p;
+  }
+  sum = warp_sum(sum);
+  __syncwarp();
+  // O = P V / l: lane c accumulates columns c, c + 32, ...
+  float acc[DPL];
+#pragma unroll
+  for (int t = 0; t < DPL; ++t) acc[t] = 0.f;
+  for (int key = 0; key < kend; ++key) {
+    const float p = pr[key];
+    const float* vr = vt + key * d;
+#pragma unroll
+    for (int t = 0; t < DPL; ++t) {
+      const int c = lane + 32 * t;
+      if (c < d) acc[t] = fmaf(p, vr[c], acc[t]);
+    }
+  }
+  const float inv_l = 1.f / sum;
+#pragma unroll
+  for (int t = 0; t < DPL; ++t) {
+    const int c = lane + 32 * t;
+    if (c < d) o[(head + row) * d + c] = acc[t] * inv_l;
+  }
+  if (lane == 0) lse[head + row] = mx + logf(sum);
+}
+
+template <int DPL, bool CAUSAL>
+int launch_simt_small(const float* q, const float* k, const float* v, float* o, float* lse, int BH, int N, int d,
+                      float scale, const LaunchCtx& ctx) {
+  const size_t smem = small_smem_bytes(N, d);
+  auto kernel = fa_fwd_simt_small_kernel<DPL, CAUSAL>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return static_cast<int>(e);
+  }
+  const dim3 grid((N + kSmallWarps - 1) / kSmallWarps, BH);
+  kernel<<<grid, kSmallWarps * 32, smem, ctx.stream>>>(q, k, v, o, lse, N, d, scale);
+  return static_cast<int>(cudaGetLastError());
+}
+
 template <int DPL, bool CAUSAL>
 int launch_simt_impl(const float* q, const float* k, const float* v, float* o, float* lse, int BH, int N, int d,
                      float scale, const LaunchCtx& ctx) {
@@ -157,9 +265,18 @@ int launch_simt_impl(const float* q, const float* k, const float* v, float* o, f
   return static_cast<int>(cudaGetLastError());
 }
 
+// Problems whose K and V fit in 64 KB of shared memory take the whole-head kernel.
+constexpr size_t kSmallSmemLimit = 64 * 1024;
+
 template <bool CAUSAL>
 int launch_simt_dpl(const float* q, const float* k, const float* v, float* o, float* lse, int BH, int N, int d,
                     float scale, const LaunchCtx& ctx) {
+  if (small_smem_bytes(N, d) <= kSmallSmemLimit) {
+    if (d <= 32) return launch_simt_small<1, CAUSAL>(q, k, v, o, lse, BH, N, d, scale, ctx);
+    if (d <= 64) return launch_simt_small<2, CAUSAL>(q, k, v, o, lse, BH, N, d, scale, ctx);
+    if (d <= 128) return launch_simt_small<4, CAUSAL>(q, k, v, o, lse, BH, N, d, scale, ctx);
+    return launch_simt_small<8, CAUSAL>(q, k, v, o, lse, BH, N, d, scale, ctx);
+  }
   if (d <= 32) return launch_simt_impl<1, CAUSAL>(q, k, v, o, lse, BH, N, d, scale, ctx);
   if (d <= 64) return launch_simt_impl<2, CAUSAL>(q, k, v, o, lse, BH, N, d, scale, ctx);
   if (d <= 128) return launch_simt_impl<4, CAUSAL>(q, k, v, o, lse, BH, N, d, scale, ctx);
