@@ -645,12 +645,19 @@ __device__ __forceinline__ void tc_softmax(const TcParams& p, const TcBars<D>& b
       const float m_new = fmaxf(m, rmax * sl2);
       // alpha = exp2(m_old - m_new): 0 on the first tile, exactly 1 when the max did not grow.
       const float alpha = (m_new == -INFINITY) ? 1.f : ex2(m - m_new);
+      float nb = (m_new == -INFINITY) ? 0.f : -m_new;
       if (j > 0) {
-        alpha_s[(a_pub & 1) * 128 + r] = alpha;
+        float* slot = alpha_s + (a_pub & 1) * 128 + r;
+        *slot = alpha;
         warp_arrive(bar.a_full(ot, a_pub & 1));
         ++a_pub;
+        // The exponentials below are made to depend on a load that follows the
+        // arrival (alpha read back, times zero: alpha is finite), so the
+        // arrival is issued before them and the correction warpgroup rescales
+        // O while they run; otherwise the compiler may schedule the arrival
+        // after the exponentials, since nothing in this warp depends on it.
+        nb = fmaf(0.f, ld_shared_volatile(slot), nb);
       }
-      const float nb = (m_new == -INFINITY) ? 0.f : -m_new;
       const uint64_t nb2 = f2_pack(nb, nb);
       uint64_t acc[4];
 #pragma unroll
