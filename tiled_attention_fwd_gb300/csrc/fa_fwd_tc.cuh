@@ -566,6 +566,14 @@ __device__ __forceinline__ void tc_mma(const TcParams& p, const TcBars<D>& bar, 
 }
 
 // ------------------------------------------------------------------ softmax
+// Shared-memory load that the compiler keeps in program order with the
+// surrounding barrier operations.
+__device__ __forceinline__ float ld_shared_volatile(const float* p) {
+  float v;
+  asm volatile("ld.volatile.shared.f32 %0, [%1];" : "=f"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+
 template <int D, bool CAUSAL>
 __device__ __forceinline__ void tc_softmax(const TcParams& p, const TcBars<D>& bar, uint8_t* gbase, uint32_t tmem,
                                            int wg, int quarter, int lane, const WaitGuard& g) {

@@ -121,14 +121,6 @@ __device__ __forceinline__ void warp_arrive(uint32_t bar) {
   if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
-// Shared-memory load that the compiler keeps in program order with the
-// surrounding barrier operations.
-__device__ __forceinline__ float ld_shared_volatile(const float* p) {
-  float v;
-  asm volatile("ld.volatile.shared.f32 %0, [%1];" : "=f"(v) : "r"(smem_u32(p)) : "memory");
-  return v;
-}
-
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
