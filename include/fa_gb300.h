@@ -248,6 +248,20 @@ int fa_status(void* stream);
  */
 int fa_set_wait_limit_ms(int ms);
 
+/*
+ * fa_selftest_wait - diagnostic of the bounded device-side waits; the pages
+ * have no counterpart (the waits and their time limit are this library's
+ * failure handling).  Enqueues on `stream` one block whose warps wait, through
+ * the attention kernels' own bounded-wait code, on barriers that nothing ever
+ * signals.  After the current wait limit (fa_set_wait_limit_ms) the first
+ * wait gives up, the block's other waits return at once, FA_ERR_TIMEOUT is
+ * recorded in the device status word and the kernel ends; fa_status() then
+ * reports it (and clears the word), and the device stays usable.  The kernel
+ * holds no tensor memory, issues no copies and writes no caller memory.
+ * Returns FA_OK when launched, FA_ERR_CUDA or FA_ERR_ARCH otherwise.
+ */
+int fa_selftest_wait(void* stream);
+
 /* fa_strerror - static, human-readable name of a return code. */
 const char* fa_strerror(int code);
 

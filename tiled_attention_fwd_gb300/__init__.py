@@ -7,11 +7,11 @@ only loads it and marshals arguments.  Build it with
 """
 from ._lib import (FAError, backward, check_status, declared_functions, fa_abi_version, fa_bwd, fa_bwd_strided,
                    fa_bwd_workspace_bytes, fa_fwd, fa_fwd_f32, fa_fwd_host, fa_fwd_host_workspace_bytes, fa_fwd_noalloc, fa_fwd_strided,
-                   fa_set_wait_limit_ms, fa_status, fa_strerror, forward, load)
+                   fa_selftest_wait, fa_set_wait_limit_ms, fa_status, fa_strerror, forward, load)
 
 __all__ = [
     "FAError", "backward", "check_status", "declared_functions", "fa_abi_version", "fa_bwd", "fa_bwd_strided",
     "fa_bwd_workspace_bytes",
     "fa_fwd", "fa_fwd_f32", "fa_fwd_host", "fa_fwd_strided",
-    "fa_fwd_host_workspace_bytes", "fa_fwd_noalloc", "fa_set_wait_limit_ms", "fa_status", "fa_strerror", "forward", "load",
+    "fa_fwd_host_workspace_bytes", "fa_fwd_noalloc", "fa_selftest_wait", "fa_set_wait_limit_ms", "fa_status", "fa_strerror", "forward", "load",
 ]

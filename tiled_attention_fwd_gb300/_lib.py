@@ -31,6 +31,7 @@ _SIGNATURES = {
     "fa_bwd_strided": (_c_int, [_c_void_p] * 9 + [_c_int] * 5 + [_c_void_p, _c_float, _c_int, _c_void_p, _c_size_t,
                                                                   _c_void_p]),
     "fa_status": (_c_int, [_c_void_p]),
+    "fa_selftest_wait": (_c_int, [_c_void_p]),
     "fa_set_wait_limit_ms": (_c_int, [_c_int]),
     "fa_strerror": (ctypes.c_char_p, [_c_int]),
     "fa_abi_version": (_c_int, []),
@@ -148,6 +149,11 @@ def fa_bwd_strided(q, k, v, o, lse, dout, dq, dk, dv, B, H, Nq, Nk, d, strides, 
 
 def fa_status(stream) -> int:
     return load().fa_status(stream)
+
+
+def fa_selftest_wait(stream) -> int:
+    """Enqueue the bounded-wait diagnostic (every wait expires after the current limit)."""
+    return load().fa_selftest_wait(stream)
 
 
 def fa_set_wait_limit_ms(ms: int) -> int:

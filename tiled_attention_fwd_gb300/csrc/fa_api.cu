@@ -474,6 +474,13 @@ int fa_status(void* stream) {
   return FA_OK;
 }
 
+int fa_selftest_wait(void* stream) {
+  fa::DeviceState* s = nullptr;
+  int rc = fa::current_device_state(&s);
+  if (rc != FA_OK) return rc;
+  return fa::launch_selftest_wait(fa::make_ctx(*s, stream)) == 0 ? FA_OK : FA_ERR_CUDA;
+}
+
 int fa_set_wait_limit_ms(int ms) {
   if (ms < 1) ms = 1;
   return fa::g_wait_limit_ms.exchange(ms);

@@ -66,6 +66,10 @@ int load_tensor_map_encoder();
 // Current time limit of the device-side waits (fa_set_wait_limit_ms), in nanoseconds.
 unsigned long long wait_limit_ns();
 
+// Diagnostic of the bounded waits (fa_selftest.cu): one block whose waits all
+// expire after ctx.limit_ns; returns a cudaError_t-like code (0 = launched).
+int launch_selftest_wait(const LaunchCtx& ctx);
+
 // bf16 tensor-core forward for one head dimension; returns a cudaError_t-like
 // code (0 = launched).  Defined in fa_tc_d<D>.cu.
 int launch_tc_d32(const FwdArgs& a, const LaunchCtx& ctx);
