@@ -743,18 +743,29 @@ __device__ __forceinline__ void tc_correction(const TcParams& p, const CUtensorM
       tc_fence_after();
       const uint32_t to = tmem + lane_off + C::TM_O + t * D;
       const uint64_t a2 = f2_pack(alpha, alpha);
+      // Chunks of 32 columns in flight per TMEM round trip: single-tile mode
+      // (d = 256, no register split, 160 registers a thread) rescales its 256
+      // columns in two round trips instead of eight; the two-tile kernels have
+      // 80 registers in this warpgroup and keep one chunk.
+      constexpr int RG = (C::NQT == 1) ? 4 : 1;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(to + c * 32, v);
-        tmem_wait_ld(v);
+      for (int c = 0; c < D / 32; c += RG) {
+        uint32_t v[RG][32];
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float2 y = f2_unpack(f2_mul(f2_pack(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), a2));
-          v[i] = __float_as_uint(y.x);
-          v[i + 1] = __float_as_uint(y.y);
+        for (int k = 0; k < RG; ++k) tmem_ld32(to + (c + k) * 32, v[k]);
+#pragma unroll
+        for (int k = 0; k < RG; ++k) tmem_wait_ld(v[k]);
+#pragma unroll
+        for (int k = 0; k < RG; ++k) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const float2 y = f2_unpack(f2_mul(f2_pack(__uint_as_float(v[k][i]), __uint_as_float(v[k][i + 1])), a2));
+            v[k][i] = __float_as_uint(y.x);
+            v[k][i + 1] = __float_as_uint(y.y);
+          }
         }
-        tmem_st32(to + c * 32, v);
+#pragma unroll
+        for (int k = 0; k < RG; ++k) tmem_st32(to + (c + k) * 32, v[k]);
       }
       tmem_wait_st();
     }
