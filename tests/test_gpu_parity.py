@@ -27,7 +27,9 @@ def test_f32_workload(name):
     _assert(check_full(WORKLOADS[name]), name)
 
 
-@pytest.mark.parametrize("N,d", [(1, 16), (2, 1), (37, 7), (129, 33), (300, 64), (64, 128), (97, 256), (1000, 16)])
+# N = 121 and 122 at d = 64 sit on either side of the whole-head kernel's 64 KB shared-memory limit.
+@pytest.mark.parametrize("N,d", [(1, 16), (2, 1), (37, 7), (129, 33), (300, 64), (64, 128), (97, 256), (1000, 16),
+                                 (121, 64), (122, 64)])
 @pytest.mark.parametrize("causal", [False, True])
 def test_f32_shapes(N, d, causal):
     w = Workload("f32_edge", 2, 3, N, d, "f32", causal, seed=100 + N + d)
