@@ -99,6 +99,12 @@ int fa_fwd_strided(const void* q, const void* k, const void* v, void* o, float* 
 
 /*
  * fa_fwd_f32 - fp32 forward pass on the CUDA cores (SIMT), all arithmetic in fp32.
+ * Same computation as fa_fwd (the plain attention of "FlashAttention-2 from
+ * PyTorch to Triton", section "What We Are Building").  Problems whose K and V
+ * of one head fit in 64 KB of shared memory (with a score row per warp) run a
+ * whole-head kernel with an exact two-pass softmax; larger ones the tiled
+ * kernel with the online-softmax rescaling of "Writing a FlashAttention kernel
+ * in Metal" (section "Online softmax").
  *
  *   q, k, v, o : device pointers to fp32 [B][H][N][d] (4-byte aligned suffices).
  *   lse        : device pointer to fp32 [B][H][N].
