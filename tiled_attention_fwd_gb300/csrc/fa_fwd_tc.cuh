@@ -59,10 +59,6 @@ struct TcParams {
   int total_units;       // BH * n_qb
   float scale_log2;      // softmax scale * log2(e)
   float* lse;            // [BH][Nq], contiguous
-  // O(b, h, row, :) at o + b * o_sb + h * o_sh + row * o_sn (d contiguous); the
-  // kernels with EPI_TMA write it through its tensor map instead.
-  __nv_bfloat16* o;
-  long long o_sb, o_sh, o_sn;
   int* status;           // device status word
   unsigned long long limit_ns;  // time limit of each device-side wait
 };
@@ -88,13 +84,12 @@ struct TcCfg {
   // A K/V stage holds two tiles: V_j and K_{j+LA} (the first stage of a unit: K_0 .. K_{LA-1}).
   static constexpr int STAGE = 2 * KV_TILE;
   // Epilogue staging: per correction warp OSTB buffers of 32 rows x 32 bf16
-  // columns (64-byte swizzled), the source boxes of the TMA stores of O.
-  // d = 64 keeps direct 16-byte stores from registers: there the staged
-  // stores measured slower.
-  static constexpr bool EPI_TMA = (D != 64);
+  // columns (64-byte swizzled), the source boxes of the TMA stores of O.  Every
+  // head dimension stages (at d = 64 the staged TMA stores measured 1-2 %
+  // faster than direct 16-byte stores from registers).
   static constexpr int OSTB = 3;
   static constexpr int OST_BUF = 32 * 64;
-  static constexpr int OST = EPI_TMA ? 4 * OSTB * OST_BUF : 0;
+  static constexpr int OST = 4 * OSTB * OST_BUF;
   static constexpr int NST_FIT = (SMEM_LIMIT - 1024 - MISC - OST - NQT * Q_TILE) / STAGE;
   static constexpr int NST = NST_FIT > 4 ? 4 : NST_FIT;  // K/V stages
   static constexpr int OFF_Q = 0;
@@ -812,7 +807,7 @@ __device__ __forceinline__ void tc_correction(const TcParams& p, const CUtensorM
         const float2 y = f2_unpack(f2_mul(f2_pack(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), il2));
         packed[i] = pack_bf16x2(y.x, y.y);
       }
-      if constexpr (C::EPI_TMA) {
+      {
         const uint32_t buf = ost + (ost_n % C::OSTB) * C::OST_BUF;
         ++ost_n;
         if (lane == 0) bulk_wait_group_read<C::OSTB - 1>();
@@ -831,16 +826,6 @@ __device__ __forceinline__ void tc_correction(const TcParams& p, const CUtensorM
             tma_store_3d(tm_o, buf, c * 32, wrow0, w.bh);
           bulk_commit_group();
         }
-      } else if (row < p.Nq) {
-        __nv_bfloat16* orow;
-        if constexpr (STRIDED)
-          orow = p.o + (w.bh / p.H) * p.o_sb + (w.bh % p.H) * p.o_sh + static_cast<long long>(row) * p.o_sn;
-        else
-          orow = p.o + (static_cast<size_t>(w.bh) * p.Nq + row) * D;
-        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
       }
     }
     if (row < p.Nq) p.lse[static_cast<size_t>(w.bh) * p.Nq + row] = (mrow + log2f(lrow)) * 0.69314718055994531f;
@@ -861,7 +846,7 @@ __device__ __forceinline__ void tc_correction(const TcParams& p, const CUtensorM
     }
   }
   // The staged O tiles must be written (and their shared memory read) before the CTA exits.
-  if (C::EPI_TMA && lane == 0) bulk_wait_group_all();
+  if (lane == 0) bulk_wait_group_all();
   __syncwarp();
 }
 

@@ -53,10 +53,6 @@ int launch_tc_impl(const FwdArgs& a, const LaunchCtx& ctx) {
   p.total_units = p.BH * p.n_qb;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.lse = a.lse;
-  p.o = static_cast<__nv_bfloat16*>(a.o);
-  p.o_sb = a.os[0];
-  p.o_sh = a.os[1];
-  p.o_sn = a.os[2];
   p.status = ctx.status;
   p.limit_ns = ctx.limit_ns;
   const int grid = p.total_units < ctx.num_sms ? p.total_units : ctx.num_sms;
