@@ -50,6 +50,15 @@ def test_bf16_ragged(d, N, causal):
     _assert(check_full(w), f"bf16 N={N} d={d} causal={causal}")
 
 
+@pytest.mark.parametrize("d", [32, 64, 128])
+@pytest.mark.parametrize("N", [1, 129, 257, 600])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_ragged_two_tile_units(d, N, causal):
+    """Enough heads that the two-tile kernel runs (small problems take the single-tile one)."""
+    w = Workload("bf16_edge_2t", 1, 160, N, d, "bf16", causal, seed=11 * N + d)
+    _assert(check_full(w), f"bf16 two-tile N={N} d={d} causal={causal}")
+
+
 @pytest.mark.parametrize("d", [32, 64, 128, 256])
 def test_bf16_large_logits_several_units(d):
     """Q, K ~ N(0, 3^2): large logits, the running max moves often (rescale path)."""

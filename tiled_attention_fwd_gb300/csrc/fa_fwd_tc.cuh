@@ -63,10 +63,13 @@ struct TcParams {
   unsigned long long limit_ns;  // time limit of each device-side wait
 };
 
-template <int D>
+// NQ: query tiles per work unit.  Two tiles (d <= 128) share every K/V tile;
+// one tile with double-buffered S serves d = 256 and, at d <= 128, problems
+// with too few 256-row units to occupy the SMs.
+template <int D, int NQ = (D <= 128 ? 2 : 1)>
 struct TcCfg {
   static constexpr int BQ = 128;                       // query rows per tile (= TMEM lanes)
-  static constexpr int NQT = (D <= 128) ? 2 : 1;       // query tiles per work unit
+  static constexpr int NQT = NQ;                       // query tiles per work unit
   static constexpr int BK = (D <= 128) ? 128 : 64;     // keys per K/V tile
   static constexpr int LA = (NQT == 1) ? 2 : 1;        // K tiles needed before the first P V
   static constexpr int SWB = (D * 2 >= 128) ? 128 : D * 2;  // swizzle span in bytes
@@ -119,18 +122,24 @@ struct TcCfg {
   static constexpr int MMA_WARP = SOFTMAX_WARPS + 4;
   static constexpr int LOAD_WARP = MMA_WARP + 1;
   static constexpr int THREADS = 32 * (SOFTMAX_WARPS + 8);  // + correction WG + MMA/TMA WG
-  // Register split (d <= 128, 512 threads launched at 128 registers each):
-  // softmax 176 and 160 between the correction and the MMA/TMA warpgroups:
-  // 80 / 80, or 72 / 88 where that measured faster (contiguous d = 64; the
-  // strided epilogue needs the correction's 80).  2*128*176 + 128*160 = 65536.
-  static constexpr bool SPLIT_REGS = (NQT == 2);
-  static constexpr uint32_t REG_SOFTMAX = 176;
-  static constexpr uint32_t REG_CORR_OTHER = 160;
-  static constexpr __host__ __device__ uint32_t reg_corr(bool strided) { return (!strided && D == 64) ? 72 : 80; }
+  // Register split (d <= 128).  Two tiles, 512 threads launched at 128
+  // registers each: softmax 176 and 160 between the correction and the
+  // MMA/TMA warpgroups: 80 / 80, or 72 / 88 where that measured faster
+  // (contiguous d = 64; the strided epilogue needs the correction's 80);
+  // 2*128*176 + 128*160 = 65536.  One tile, 384 threads launched at 168:
+  // softmax 208, correction 152, MMA/TMA 144; 128*(208 + 296) = 64512.
+  // d = 256 (one tile, 64-column S) fits 168 everywhere and is not split.
+  static constexpr bool SPLIT_REGS = (D <= 128);
+  static constexpr uint32_t REG_SOFTMAX = (NQT == 2) ? 176 : 208;
+  static constexpr uint32_t REG_CORR_OTHER = (NQT == 2) ? 160 : 296;
+  static constexpr __host__ __device__ uint32_t reg_corr(bool strided) {
+    return NQT == 1 ? 152 : ((!strided && D == 64) ? 72 : 80);
+  }
   static constexpr int LAUNCH_REGS = 65536 / THREADS > 255 ? 255 : (65536 / THREADS) & ~7;
-  static_assert(!SPLIT_REGS || 2 * 128 * REG_SOFTMAX + 128 * REG_CORR_OTHER <= THREADS * LAUNCH_REGS,
+  static_assert(!SPLIT_REGS || NQT * 128 * REG_SOFTMAX + 128 * REG_CORR_OTHER <= THREADS * LAUNCH_REGS,
                 "register split exceeds the launch budget");
   static_assert(D == 32 || D == 64 || D == 128 || D == 256, "head dim");
+  static_assert(NQ == 1 || (NQ == 2 && D <= 128), "query tiles per unit");
   static_assert(NST >= 2, "K/V stages");
   static_assert(LA <= 2, "a stage holds at most two K tiles");
   static_assert((D == 256) ? (TM_S + 2 * TM_SB <= TM_COLS && NO * D <= TM_S)
@@ -145,9 +154,9 @@ struct TcUnit {
   int nmax;
 };
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, int NQ>
 __device__ __forceinline__ TcUnit tc_decode(int u, const TcParams& p) {
-  using C = TcCfg<D>;
+  using C = TcCfg<D, NQ>;
   TcUnit w;
   const int qb = p.n_qb - 1 - u / p.BH;  // heaviest query blocks first
   w.bh = u % p.BH;
@@ -193,9 +202,9 @@ __device__ __forceinline__ bool wait_bar_drain(uint32_t bar, uint32_t parity, co
 }
 
 // Barrier addresses in shared memory.
-template <int D>
+template <int D, int NQ>
 struct TcBars {
-  using C = TcCfg<D>;
+  using C = TcCfg<D, NQ>;
   uint32_t b0;
   // Q tile t loaded / free again (one phase per work unit).
   __device__ __forceinline__ uint32_t q_full(int t) const { return b0 + 8u * t; }
@@ -232,11 +241,11 @@ struct TcBars {
 // as soon as the current unit's last S_t product has completed (q_empty(t)).
 //
 // Single-tile mode: per unit, Q, then {K_0, K_1}, then {V_j, K_{j+2}}.
-template <int D, bool CAUSAL, bool STRIDED>
+template <int D, bool CAUSAL, bool STRIDED, int NQ>
 __device__ __forceinline__ void tc_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
-                                            const TcParams& p, const TcBars<D>& bar, uint32_t base,
+                                            const TcParams& p, const TcBars<D, NQ>& bar, uint32_t base,
                                             const WaitGuard& g) {
-  using C = TcCfg<D>;
+  using C = TcCfg<D, NQ>;
   const uint64_t pol_q = policy_evict_first();
   const uint64_t pol_kv = policy_evict_last();
   uint32_t pos = 0;       // stages issued so far
@@ -289,14 +298,14 @@ __device__ __forceinline__ void tc_producer(const CUtensorMap* tm_q, const CUten
     int uk = 0;
     int u = tc_unit(0);
     if (u < p.total_units) {
-      TcUnit w = tc_decode<D, CAUSAL>(u, p);
+      TcUnit w = tc_decode<D, CAUSAL, NQ>(u, p);
       uint32_t s0, full;
       ok = load_q(w, 0) && stage_begin(1, s0, full);
       if (ok) load_tile(tm_k, s0, full, 0, w.bh);
       while (ok) {
         const int un = tc_unit(uk + 1);
         const bool has_next = un < p.total_units;
-        const TcUnit wn = tc_decode<D, CAUSAL>(has_next ? un : u, p);
+        const TcUnit wn = tc_decode<D, CAUSAL, NQ>(has_next ? un : u, p);
         for (int j = 0; ok && j < w.nmax; ++j) {
           const bool k_here = j + 1 < w.nmax;
           const bool k_next = !k_here && has_next;
@@ -314,7 +323,7 @@ __device__ __forceinline__ void tc_producer(const CUtensorMap* tm_q, const CUten
     }
   } else {
     for (int uk = 0, u; ok && (u = tc_unit(uk)) < p.total_units; ++uk) {
-      const TcUnit w = tc_decode<D, CAUSAL>(u, p);
+      const TcUnit w = tc_decode<D, CAUSAL, NQ>(u, p);
       if (!(ok = load_q(w, uk))) break;
       uint32_t s0, full;
       for (int t = -1; t < w.nmax; ++t) {
@@ -354,9 +363,9 @@ __device__ __forceinline__ void tc_producer(const CUtensorMap* tm_q, const CUten
 // Descriptors are kept as (low, high) words and built once: a tile position
 // or K step only adds a constant to the low word's address field (bits 0..13
 // hold address / 16, and no shared address reaches 2^18, so it never carries).
-template <int D>
+template <int D, int NQ>
 struct TcMma {
-  using C = TcCfg<D>;
+  using C = TcCfg<D, NQ>;
   static constexpr uint32_t IDESC_QK = make_idesc_bf16(128, C::BK, 0);
   static constexpr uint32_t IDESC_PV = make_idesc_bf16(128, D, 1);
   // K-major (Q, K) and MN-major (V) operands share the stride byte offset
@@ -428,11 +437,11 @@ struct TcMma {
   __device__ __forceinline__ void commit(uint32_t bar) const { mma_commit_elect(bar); }
 };
 
-template <int D, bool CAUSAL>
-__device__ __forceinline__ void tc_mma(const TcParams& p, const TcBars<D>& bar, uint32_t base, uint32_t tmem,
+template <int D, bool CAUSAL, int NQ>
+__device__ __forceinline__ void tc_mma(const TcParams& p, const TcBars<D, NQ>& bar, uint32_t base, uint32_t tmem,
                                        const WaitGuard& g) {
-  using C = TcCfg<D>;
-  const TcMma<D> M(tmem, base);
+  using C = TcCfg<D, NQ>;
+  const TcMma<D, NQ> M(tmem, base);
   // Every lane waits (a non-blocking test first, then the bounded wait); the
   // outcome is made warp-uniform.
   auto wait = [&](uint32_t b, uint32_t par) -> bool {
@@ -496,14 +505,14 @@ __device__ __forceinline__ void tc_mma(const TcParams& p, const TcBars<D>& bar, 
       return true;
     };
     if (u < p.total_units) {
-      TcUnit w = tc_decode<D, CAUSAL>(u, p);
+      TcUnit w = tc_decode<D, CAUSAL, NQ>(u, p);
       uint32_t st;
       ok = stage_acquire(st) && first_qk(w, 0, 0, 2 * st) && first_qk(w, 0, 1, 2 * st);
       if (ok) M.commit(bar.kv_empty(st));
       while (ok) {
         const int un = tc_unit(uk + 1);
         const bool has_next = un < p.total_units;
-        const TcUnit wn = tc_decode<D, CAUSAL>(has_next ? un : u, p);
+        const TcUnit wn = tc_decode<D, CAUSAL, NQ>(has_next ? un : u, p);
         for (int j = 0; ok && j < w.nmax; ++j) {
           if (!(ok = stage_acquire(st))) break;
           // In a unit's last step both P V products go first: the next unit's
@@ -525,7 +534,7 @@ __device__ __forceinline__ void tc_mma(const TcParams& p, const TcBars<D>& bar, 
   } else {
     uint32_t qk_total = 0;  // S products issued so far
     for (int uk = 0, u; ok && (u = tc_unit(uk)) < p.total_units; ++uk) {
-      const TcUnit w = tc_decode<D, CAUSAL>(u, p);
+      const TcUnit w = tc_decode<D, CAUSAL, NQ>(u, p);
       if (!(ok = wait(bar.q_full(0), uk & 1))) break;
       uint32_t st;
       if (!(ok = stage_acquire(st))) break;
@@ -569,10 +578,10 @@ __device__ __forceinline__ float ld_shared_volatile(const float* p) {
   return v;
 }
 
-template <int D, bool CAUSAL>
-__device__ __forceinline__ void tc_softmax(const TcParams& p, const TcBars<D>& bar, uint8_t* gbase, uint32_t tmem,
+template <int D, bool CAUSAL, int NQ>
+__device__ __forceinline__ void tc_softmax(const TcParams& p, const TcBars<D, NQ>& bar, uint8_t* gbase, uint32_t tmem,
                                            int wg, int quarter, int lane, const WaitGuard& g) {
-  using C = TcCfg<D>;
+  using C = TcCfg<D, NQ>;
   const int r = quarter * 32 + lane;  // row within the query tile = TMEM lane
   const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
   const int ot = (C::NQT == 2) ? wg : 0;
@@ -589,7 +598,7 @@ __device__ __forceinline__ void tc_softmax(const TcParams& p, const TcBars<D>& b
   bool ok = true;
 
   for (int uk = 0, u; ok && (u = tc_unit(uk)) < p.total_units; ++uk) {
-    const TcUnit w = tc_decode<D, CAUSAL>(u, p);
+    const TcUnit w = tc_decode<D, CAUSAL, NQ>(u, p);
     const int n = w.n[wg];
     if (n == 0) continue;
     const int row0 = w.row0 + wg * C::BQ;
@@ -697,11 +706,11 @@ __device__ __forceinline__ void tc_softmax(const TcParams& p, const TcBars<D>& b
 }
 
 // ------------------------------------------------------------------ correction + epilogue
-template <int D, bool CAUSAL, bool STRIDED>
-__device__ __forceinline__ void tc_correction(const TcParams& p, const CUtensorMap* tm_o, const TcBars<D>& bar,
+template <int D, bool CAUSAL, bool STRIDED, int NQ>
+__device__ __forceinline__ void tc_correction(const TcParams& p, const CUtensorMap* tm_o, const TcBars<D, NQ>& bar,
                                               uint8_t* gbase, uint32_t tmem, int quarter, int lane,
                                               const WaitGuard& g) {
-  using C = TcCfg<D>;
+  using C = TcCfg<D, NQ>;
   const int r = quarter * 32 + lane;
   const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
   const float* alpha_base = reinterpret_cast<const float*>(gbase + C::OFF_ALPHA);
@@ -742,7 +751,7 @@ __device__ __forceinline__ void tc_correction(const TcParams& p, const CUtensorM
       // (d = 256, no register split, 160 registers a thread) rescales its 256
       // columns in two round trips instead of eight; the two-tile kernels have
       // 80 registers in this warpgroup and keep one chunk.
-      constexpr int RG = (C::NQT == 1) ? 4 : 1;
+      constexpr int RG = (C::NQT == 1) ? (D / 32 < 4 ? D / 32 : 4) : 1;
 #pragma unroll 1
       for (int c = 0; c < D / 32; c += RG) {
         uint32_t v[RG][32];
@@ -836,7 +845,7 @@ __device__ __forceinline__ void tc_correction(const TcParams& p, const CUtensorM
   release_o(0);
   if (C::NO == 2) release_o(1);
   for (int uk = 0, u; ok && (u = tc_unit(uk)) < p.total_units; ++uk) {
-    const TcUnit w = tc_decode<D, CAUSAL>(u, p);
+    const TcUnit w = tc_decode<D, CAUSAL, NQ>(u, p);
     // Same order as the MMA warp's P V products: (tile 0, j), (tile 1, j), (tile 0, j+1), ...
     for (int j = 0; ok && j < w.nmax; ++j) {
       if (ok && j >= 1 && j < w.n[0]) ok = rescale(0, a_cnt0, od0);
@@ -851,19 +860,19 @@ __device__ __forceinline__ void tc_correction(const TcParams& p, const CUtensorM
 }
 
 // ------------------------------------------------------------------ kernel
-template <int D, bool CAUSAL, bool STRIDED>
-__global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
+template <int D, bool CAUSAL, bool STRIDED, int NQ>
+__global__ void __launch_bounds__(TcCfg<D, NQ>::THREADS, 1)
     fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                      const TcParams p) {
-  using C = TcCfg<D>;
+  using C = TcCfg<D, NQ>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const TcBars<D> bar{base + C::OFF_BAR};
+  const TcBars<D, NQ> bar{base + C::OFF_BAR};
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::OFF_TMEM_SLOT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::OFF_ABORT);
 
@@ -908,14 +917,14 @@ __global__ void __launch_bounds__(TcCfg<D>::THREADS, 1)
 
   if (warp < C::SOFTMAX_WARPS) {
     if constexpr (C::SPLIT_REGS) regs_increase<C::REG_SOFTMAX>();
-    tc_softmax<D, CAUSAL>(p, bar, gbase, tmem, warp >> 2, warp & 3, lane, g);
+    tc_softmax<D, CAUSAL, NQ>(p, bar, gbase, tmem, warp >> 2, warp & 3, lane, g);
   } else if (warp < C::SOFTMAX_WARPS + 4) {
     if constexpr (C::SPLIT_REGS) regs_decrease<C::reg_corr(STRIDED)>();
-    tc_correction<D, CAUSAL, STRIDED>(p, &tm_o, bar, gbase, tmem, warp & 3, lane, g);
+    tc_correction<D, CAUSAL, STRIDED, NQ>(p, &tm_o, bar, gbase, tmem, warp & 3, lane, g);
   } else {
     if constexpr (C::SPLIT_REGS) regs_decrease<C::REG_CORR_OTHER - C::reg_corr(STRIDED)>();
-    if (warp == C::LOAD_WARP && lane == 0) tc_producer<D, CAUSAL, STRIDED>(&tm_q, &tm_k, &tm_v, p, bar, base, g);
-    if (warp == C::MMA_WARP) tc_mma<D, CAUSAL>(p, bar, base, tmem, g);
+    if (warp == C::LOAD_WARP && lane == 0) tc_producer<D, CAUSAL, STRIDED, NQ>(&tm_q, &tm_k, &tm_v, p, bar, base, g);
+    if (warp == C::MMA_WARP) tc_mma<D, CAUSAL, NQ>(p, bar, base, tmem, g);
   }
 
   __syncwarp();

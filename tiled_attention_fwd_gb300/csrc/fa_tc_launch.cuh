@@ -9,10 +9,10 @@
 
 namespace fa {
 
-template <int D, bool CAUSAL, bool STRIDED>
+template <int D, bool CAUSAL, bool STRIDED, int NQ = TcCfg<D>::NQT>
 int launch_tc_impl(const FwdArgs& a, const LaunchCtx& ctx) {
-  using C = TcCfg<D>;
-  auto kernel = fa_fwd_tc_kernel<D, CAUSAL, STRIDED>;
+  using C = TcCfg<D, NQ>;
+  auto kernel = fa_fwd_tc_kernel<D, CAUSAL, STRIDED, NQ>;
   if constexpr (C::SPLIT_REGS) {
     // The warpgroups re-split the registers the block was launched with
     // (setmaxnreg); the split is sized for exactly LAUNCH_REGS per thread.  A
@@ -62,11 +62,28 @@ int launch_tc_impl(const FwdArgs& a, const LaunchCtx& ctx) {
 
 }  // namespace fa
 
+namespace fa {
+
+// Contiguous tensors at d <= 128 take the single-tile kernel (128-row work
+// units, S double-buffered) when even 128-row units would not outnumber the
+// SMs: there the two-tile kernel leaves most SMs idle and the one-tile chain
+// per key tile is shorter.
+template <int D, bool CAUSAL>
+int launch_tc_contiguous(const FwdArgs& a, const LaunchCtx& ctx) {
+  if constexpr (D <= 128) {
+    const long long units = static_cast<long long>(a.B) * a.H * ((a.Nq + 255) / 256);
+    if (2 * units <= ctx.num_sms) return launch_tc_impl<D, CAUSAL, false, 1>(a, ctx);
+  }
+  return launch_tc_impl<D, CAUSAL, false>(a, ctx);
+}
+
+}  // namespace fa
+
 // Contiguous [B][H][N][d] tensors (3-D maps, the fast path), in fa_tc_d<D>.cu.
 #define FA_DEFINE_TC_LAUNCHER(DIM)                                                                     \
   namespace fa {                                                                                       \
   int launch_tc_d##DIM(const FwdArgs& a, const LaunchCtx& ctx) {                                       \
-    return a.causal ? launch_tc_impl<DIM, true, false>(a, ctx) : launch_tc_impl<DIM, false, false>(a, ctx); \
+    return a.causal ? launch_tc_contiguous<DIM, true>(a, ctx) : launch_tc_contiguous<DIM, false>(a, ctx); \
   }                                                                                                    \
   }
 
