@@ -42,6 +42,15 @@ def test_rectangular_matches_oracle(B, H, Nq, Nk, d, causal):
 
 
 @pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+@pytest.mark.parametrize("B,H,Nq,Nk,d", [
+    (1, 160, 100, 300, 128), (1, 160, 777, 129, 64), (1, 160, 129, 513, 32), (1, 160, 513, 1, 128),
+])
+def test_rectangular_two_tile_units(B, H, Nq, Nk, d, causal):
+    """Enough heads that the two-tile kernel runs (small problems take the single-tile one)."""
+    test_rectangular_matches_oracle(B, H, Nq, Nk, d, causal)
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
 @pytest.mark.parametrize("d", [64, 128, 256])
 def test_bshd_layout_matches_oracle(d, causal):
     """Q, K, V and O stored as [B, N, H, d] (rows of one head H*d apart), passed as [B, H, N, d] views."""

@@ -64,17 +64,17 @@ int launch_tc_impl(const FwdArgs& a, const LaunchCtx& ctx) {
 
 namespace fa {
 
-// Contiguous tensors at d <= 128 take the single-tile kernel (128-row work
-// units, S double-buffered) when even 128-row units would not outnumber the
-// SMs: there the two-tile kernel leaves most SMs idle and the one-tile chain
-// per key tile is shorter.
-template <int D, bool CAUSAL>
-int launch_tc_contiguous(const FwdArgs& a, const LaunchCtx& ctx) {
+// At d <= 128 the single-tile kernel (128-row work units, S double-buffered)
+// runs when even 128-row units would not outnumber the SMs: there the
+// two-tile kernel leaves most SMs idle and the one-tile chain per key tile is
+// shorter.
+template <int D, bool CAUSAL, bool STRIDED>
+int launch_tc_sized(const FwdArgs& a, const LaunchCtx& ctx) {
   if constexpr (D <= 128) {
     const long long units = static_cast<long long>(a.B) * a.H * ((a.Nq + 255) / 256);
-    if (2 * units <= ctx.num_sms) return launch_tc_impl<D, CAUSAL, false, 1>(a, ctx);
+    if (2 * units <= ctx.num_sms) return launch_tc_impl<D, CAUSAL, STRIDED, 1>(a, ctx);
   }
-  return launch_tc_impl<D, CAUSAL, false>(a, ctx);
+  return launch_tc_impl<D, CAUSAL, STRIDED>(a, ctx);
 }
 
 }  // namespace fa
@@ -83,7 +83,7 @@ int launch_tc_contiguous(const FwdArgs& a, const LaunchCtx& ctx) {
 #define FA_DEFINE_TC_LAUNCHER(DIM)                                                                     \
   namespace fa {                                                                                       \
   int launch_tc_d##DIM(const FwdArgs& a, const LaunchCtx& ctx) {                                       \
-    return a.causal ? launch_tc_contiguous<DIM, true>(a, ctx) : launch_tc_contiguous<DIM, false>(a, ctx); \
+    return a.causal ? launch_tc_sized<DIM, true, false>(a, ctx) : launch_tc_sized<DIM, false, false>(a, ctx); \
   }                                                                                                    \
   }
 
@@ -91,6 +91,6 @@ int launch_tc_contiguous(const FwdArgs& a, const LaunchCtx& ctx) {
 #define FA_DEFINE_TC_STRIDED_LAUNCHER(DIM)                                                           \
   namespace fa {                                                                                     \
   int launch_tc_strided_d##DIM(const FwdArgs& a, const LaunchCtx& ctx) {                             \
-    return a.causal ? launch_tc_impl<DIM, true, true>(a, ctx) : launch_tc_impl<DIM, false, true>(a, ctx); \
+    return a.causal ? launch_tc_sized<DIM, true, true>(a, ctx) : launch_tc_sized<DIM, false, true>(a, ctx); \
   }                                                                                                  \
   }
