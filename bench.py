@@ -85,44 +85,66 @@ def load_traffic(workload: str, prefix: str = "traffic", sources=None):
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms during the timed region."""
+    """nvidia-smi clocks / throttle reasons, one sample every `period_ms`, each
+    stamped on arrival with the host clock (time.perf_counter) by a reader
+    thread, so that the samples can be binned against the timed region.
+
+    The benchmark keeps the GPU under the same load (the same L2 flush + step
+    sequence, untimed) for a while before and after its timed steps; `sm_mhz`
+    is the median over that whole load window, which contains the timed
+    region, and the samples that fall inside the timed region itself are
+    reported separately."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, period_ms: int = 20):
         self.index = index
+        self.period_ms = period_ms
         self.proc = None
-        self.out = None
+        self.thread = None
+        self.samples = []  # (perf_counter seconds, csv row)
+        self.marks = {}
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.perf_counter(), line))
 
     def __enter__(self):
+        import threading
+
         exe = shutil.which("nvidia-smi")
         if exe is not None:
-            self.out = tempfile.TemporaryFile(mode="w+")
             self.proc = subprocess.Popen([exe, f"--id={self.index}", f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
-                                         stdout=self.out, stderr=subprocess.DEVNULL)
+                                          "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True, bufsize=1)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
             time.sleep(0.3)
         return self
 
+    def mark(self, name: str):
+        self.marks[name] = time.perf_counter()
+
     def __exit__(self, *exc):
         if self.proc is not None:
-            time.sleep(0.25)
+            time.sleep(0.1)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+            self.thread.join(timeout=5)
 
-    def summary(self):
-        if self.out is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.out.seek(0)
-        rows = [r for r in csv.reader(io.StringIO(self.out.read())) if len(r) >= 9]
+    @staticmethod
+    def _parse(rows):
         sm, smax, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
+        for line in rows:
+            r = next(csv.reader(io.StringIO(line)), [])
+            if len(r) < 9:
+                continue
             try:
                 sm.append(float(r[1]))
                 smax = float(r[2])
@@ -131,8 +153,50 @@ class ClockSampler:
             for n, val in zip(names, r[5:9]):
                 if val.strip().lower() == "active":
                     reasons.add(n)
+        return sm, smax, reasons
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        lo, hi = self.marks.get("load_start", 0.0), self.marks.get("load_end", float("inf"))
+        t0, t1 = self.marks.get("timed_start", lo), self.marks.get("timed_end", hi)
+        load = [line for t, line in self.samples if lo <= t <= hi]
+        timed = [line for t, line in self.samples if t0 <= t <= t1]
+        sm, smax, reasons = self._parse(load)
+        sm_t, _, reasons_t = self._parse(timed)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons | reasons_t), "samples": len(sm),
+                "samples_in_timed_region": len(sm_t),
+                "sm_mhz_timed_region": statistics.median(sm_t) if sm_t else None,
+                "period_ms": self.period_ms,
+                "load_window_s": (hi - lo) if hi != float("inf") else None,
+                "timed_region_s": (t1 - t0) if t1 != float("inf") else None,
+                "note": "sm_mhz: median over a window of identical load (untimed flush + step sequences before "
+                        "and after the timed steps) that contains the timed region"}
+
+
+def soak(step_fn, seconds: float, sync):
+    """Run `step_fn` back to back for about `seconds` (untimed; keeps the GPU
+    under the timed region's load while the clock sampler runs)."""
+    t_end = time.perf_counter() + seconds
+    while time.perf_counter() < t_end:
+        for _ in range(8):
+            step_fn()
+        sync()
+
+
+MUFU_EX2_PER_CLK_PER_SM = 32  # ex2.approx.ftz.f32 results per clock per SM, measured on GB300
+
+
+def exp_rate(w, kernel_ms: float, sms: int, sm_mhz):
+    """Exponentials of the softmax (one per unmasked score: B*H*N^2, halved when
+    causal) per second, against the MUFU rate at the sampled SM clock."""
+    n = float(w.B * w.H * w.N * w.N) / (2.0 if w.causal else 1.0)
+    per_s = n / (kernel_ms / 1e3)
+    mhz = sm_mhz if sm_mhz else 2070.0
+    peak = MUFU_EX2_PER_CLK_PER_SM * sms * mhz * 1e6
+    return {"per_launch": n, "per_s": per_s, "peak_per_s": peak, "frac": per_s / peak,
+            "peak_basis": f"{MUFU_EX2_PER_CLK_PER_SM} ex2/clk/SM x {sms} SMs x {mhz:.0f} MHz"}
 
 
 def aggregate_ranks(local_seconds: float, world: int, reduce_max=None) -> float:
@@ -308,8 +372,16 @@ def run_ours(args, w):
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+
+    def load_step():
+        flush.zero_()
+        step()
+
     with ClockSampler(local) as clocks:
+        clocks.mark("load_start")
+        soak(load_step, args.clock_soak_s, torch.cuda.synchronize)
         barrier()
+        clocks.mark("timed_start")
         t_wall = time.perf_counter()
         for i in range(args.steps):
             flush.zero_()  # outside the events: L2 holds no inputs when each step starts
@@ -318,6 +390,9 @@ def run_ours(args, w):
             ends[i].record(stream)
         barrier()
         t_wall = time.perf_counter() - t_wall
+        clocks.mark("timed_end")
+        soak(load_step, args.clock_soak_s / 4, torch.cuda.synchronize)
+        clocks.mark("load_end")
     fa.check_status(dev)
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     local_s = sum(step_ms) / 1e3
@@ -370,6 +445,9 @@ def run_ours(args, w):
     peaks, src = load_peaks()
     peak = peaks["bf16_tflops"]
     achieved = w.flops / (kernel_ms / 1e3) / 1e12
+    clock_rec = clocks.summary()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    exps = exp_rate(w, kernel_ms, sms, clock_rec.get("sm_mhz"))
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
             "traffic": load_traffic(w.name), "peak_source": f"bf16 dense burst, {src}",
             "kernel": f"fa_fwd_tc_kernel<{w.d},{str(w.causal).lower()}>" if w.dtype == "bf16" else "fa_fwd_simt_kernel",
@@ -380,7 +458,7 @@ def run_ours(args, w):
             "warmup": args.warmup, "ms_per_step": total_s / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
             "config": config_of(w), "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": args.steps, "clocks": clocks.summary(),
+            "gpu_launches": args.steps, "clocks": clock_rec, "exp": exps,
             "kernel_ms": {"mean": kernel_ms, "min": min(step_ms), "max": max(step_ms),
                           "median": statistics.median(step_ms)},
             "wall_s_timed_region": t_wall,
@@ -445,8 +523,16 @@ def run_ours_bwd(args, w):
     fa.check_status(dev)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+
+    def load_step():
+        flush.zero_()
+        step()
+
     with ClockSampler(local) as clocks:
+        clocks.mark("load_start")
+        soak(load_step, args.clock_soak_s, torch.cuda.synchronize)
         barrier()
+        clocks.mark("timed_start")
         t_wall = time.perf_counter()
         for i in range(args.steps):
             flush.zero_()
@@ -455,6 +541,9 @@ def run_ours_bwd(args, w):
             ends[i].record(stream)
         barrier()
         t_wall = time.perf_counter() - t_wall
+        clocks.mark("timed_end")
+        soak(load_step, args.clock_soak_s / 4, torch.cuda.synchronize)
+        clocks.mark("load_end")
     fa.check_status(dev)
     step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
     total_s = aggregate_ranks(sum(step_ms) / 1e3, world, reduce_max)
@@ -595,21 +684,24 @@ def run_report(args):
         check_status(dev)
         med = statistics.median(times)
         tflops = w.flops / (med * 1e-3) / 1e12
+        exps = exp_rate(w, med, torch.cuda.get_device_properties(dev).multi_processor_count, None)
         ora, heads, secs = oracle_sample(w, args.report_cpu_seconds, pool, cores, host)
         row = {"workload": name, "dtype": w.dtype, "causal": w.causal, "gflop": w.flops / 1e9,
                "gpu_ms_median": med, "gpu_ms_min": min(times), "gpu_ms_max": max(times), "runs": runs,
                "tflops": tflops, "frac_of_bf16_peak": tflops / peak, "peak_tflops": peak, "peak_source": peak_src,
+               "exp_per_s": exps["per_s"], "exp_frac_of_mufu": exps["frac"],
                "oracle_tflops": ora, "oracle_heads": heads, "oracle_s": secs,
                "oracle_full_s": w.flops / (ora * 1e12), "oracle_cores": cores}
         rows.append(row)
         print(json.dumps(row), flush=True)
     pool.close()
     print(f"\n| config | GFLOP | GPU median / min / max (ms, {runs} runs) | TFLOP/s | of bf16 peak | "
-          f"CPU oracle ({cores} cores): TFLOP/s | oracle s, full config |")
-    print("|---|---|---|---|---|---|---|")
+          f"exp/s (of MUFU at 2070 MHz) | CPU oracle ({cores} cores): TFLOP/s | oracle s, full config |")
+    print("|---|---|---|---|---|---|---|---|")
     for r in rows:
         print(f"| `{r['workload']}` | {r['gflop']:.3g} | {r['gpu_ms_median']:.4f} / {r['gpu_ms_min']:.4f} / "
               f"{r['gpu_ms_max']:.4f} | {r['tflops']:.4g} | {r['frac_of_bf16_peak']:.3g} | "
+              f"{r['exp_per_s']:.3g} ({r['exp_frac_of_mufu']:.3g}) | "
               f"{r['oracle_tflops']:.3g} | {r['oracle_full_s']:.3g} |")
     return 0
 
@@ -631,6 +723,9 @@ def main(argv=None):
     ap.add_argument("--report", action="store_true",
                     help="time the forward on every config beside the CPU oracle and print a table")
     ap.add_argument("--report-cpu-seconds", type=float, default=8.0, help="CPU oracle budget per config in --report")
+    ap.add_argument("--clock-soak-s", type=float, default=0.6,
+                    help="seconds of identical untimed load before the timed steps (a quarter of it after), "
+                         "so that the clock samples bracket the timed region")
     args = ap.parse_args(argv)
     if args.report:
         return run_report(args)

@@ -228,8 +228,12 @@ int fa_bwd_strided(const void* q, const void* k, const void* v, const void* o, c
  * Each call first clears the status word with cudaMemsetAsync on `stream`,
  * then launches.  All calls on a device share the one array: calls whose
  * kernels overlap on the GPU (on different streams) race on it.  A wait that
- * expires ends the kernel early as with fa_fwd, but is recorded only in this
- * shared word, which fa_status() does not read.
+ * expires ends the kernel early as with fa_fwd and is recorded in this shared
+ * word; fa_status() reads (and clears) it as well, so it reports the expiry
+ * of the latest fa_fwd_noalloc call on the device (the next call clears the
+ * word first).  fa_status allocates its own status word on its first call on
+ * a device, so a caller that may not allocate later makes that first call
+ * at set-up.
  *
  * The first call on each device does the set-up (with that device current):
  * it looks up the array's device address with cudaGetSymbolAddress, queries
@@ -241,7 +245,8 @@ int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* 
 
 /*
  * fa_status - synchronises `stream`, then reads and clears the device status
- * word of the current device.  Returns FA_OK, FA_ERR_TIMEOUT if a kernel
+ * word of the current device, and the status word of fa_fwd_noalloc's static
+ * scratch on that device.  Returns FA_OK, FA_ERR_TIMEOUT if a kernel
  * launched since the last call gave up on a bounded wait, or FA_ERR_CUDA if
  * the synchronisation itself failed.
  */

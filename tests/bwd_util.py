@@ -26,7 +26,7 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-import oracle
+from oracle_workers import head_bounds
 from tiled_attention_fwd_gb300 import backward, check_status, forward
 from tiled_attention_fwd_gb300.inputs import Workload, as_f64_numpy, make_dout, make_qkv
 
@@ -45,20 +45,6 @@ def run_cuda_fwd_bwd(q, k, v, do, causal, scale):
     dq, dk, dv = backward(qd, kd, vd, o, lse, dod, causal=causal, scale=scale)
     check_status(dev)
     return {name: as_f64_numpy(t.cpu()) for name, t in (("dq", dq), ("dk", dk), ("dv", dv), ("o", o))}
-
-
-def head_bounds(q, k, v, do, o_gpu, scale, causal):
-    """Reference gradients and the per-element magnitudes M for one head (fp64)."""
-    dq, dk, dv = oracle.attention_backward_head(q, k, v, do, scale, causal)
-    p = oracle.probabilities(oracle.scores(q, k, scale, causal))
-    o = p @ v
-    ds = p * (do @ v.T - (do * o).sum(1, keepdims=True))
-    e = np.abs(do * o_gpu).sum(1, keepdims=True)
-    pe = p * e
-    m_v = np.abs(p).T @ np.abs(do)
-    m_k = scale * (np.abs(ds).T @ np.abs(q) + pe.T @ np.abs(q))
-    m_q = scale * (np.abs(ds) @ np.abs(k) + pe @ np.abs(k))
-    return (dq, dk, dv), (m_q, m_k, m_v)
 
 
 def compare_head(got, ref, mag):

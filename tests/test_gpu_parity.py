@@ -97,13 +97,18 @@ def test_status_clean_and_deterministic():
     fa.check_status()
 
 
-def test_host_buffer_entry_point_matches_device_entry_point():
-    w = Workload("host", 1, 2, 300, 64, "bf16", False, seed=9)
+@pytest.mark.parametrize("B,H,N,d", [(1, 2, 300, 64), (3, 5, 1000, 64), (3, 5, 1000, 128), (1, 9, 517, 256)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_host_buffer_entry_point_matches_device_entry_point(B, H, N, d, causal):
+    """fa_fwd_host pipelines its copies and kernels over up to 8 chunks of heads;
+    B*H = 15 and 9 give uneven chunks (1 or 2 heads).  Every chunk runs the same
+    kernel on the same rows as fa_fwd, so the results must be identical bits."""
+    w = Workload("host", B, H, N, d, "bf16", causal, seed=9 + N + d)
     q, k, v = make_qkv(w)
     o_dev, l_dev = run_cuda(q, k, v, w.causal, w.scale)
     qp, kp, vp = (t.pin_memory() for t in (q, k, v))
-    o = torch.empty_like(qp).pin_memory()
-    lse = torch.empty(q.shape[:-1], dtype=torch.float32).pin_memory()
+    o = torch.full(q.shape, float("nan"), dtype=torch.bfloat16).pin_memory()
+    lse = torch.full(q.shape[:-1], float("nan"), dtype=torch.float32).pin_memory()
     nbytes = fa.fa_fwd_host_workspace_bytes(w.B, w.H, w.N, w.d)
     ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream().cuda_stream
@@ -111,6 +116,7 @@ def test_host_buffer_entry_point_matches_device_entry_point():
                         nbytes, w.B, w.H, w.N, w.d, w.scale, w.causal, stream)
     assert rc == 0, fa.fa_strerror(rc)
     torch.cuda.synchronize()
+    fa.check_status()
     assert np.array_equal(o.double().numpy(), o_dev) and np.array_equal(lse.double().numpy(), l_dev)
 
 

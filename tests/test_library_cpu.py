@@ -3,6 +3,7 @@ symbol the public header declares, and rejects bad arguments on the host
 before touching a device."""
 import ctypes
 import os
+import re
 import shutil
 
 import pytest
@@ -113,14 +114,21 @@ def test_tensor_core_kernels_fit_their_register_split():
     # 4 head dims x causal / not x contiguous / strided, plus the single-tile
     # kernels of d = 32, 64, 128 (causal / not, contiguous / strided)
     assert len(tc) == 28
+    # Template parameters <D, CAUSAL, STRIDED, NQ> in the mangled name.
+    pat = re.compile(r"fa_fwd_tc_kernelILi(\d+)ELb([01])ELb([01])ELi([12])E")
+    seen = set()
     for name, r in tc.items():
+        m = pat.search(name)
+        assert m, f"unrecognised kernel name {name}"
+        d, causal, strided, nq = int(m.group(1)), m.group(2), m.group(3), int(m.group(4))
+        seen.add((d, causal, strided, nq))
         assert r["spill_stores"] == 0 and r["spill_loads"] == 0, (name, r)
-        if "ILi256E" in name:
-            assert r["registers"] <= 168, (name, r)
-        elif name.split("ELb")[2].startswith("0ELi1E") or name.split("ELb")[2].startswith("1ELi1E"):
-            assert r["registers"] == 168, (name, r)
+        if d == 256:
+            assert nq == 1 and r["registers"] <= 168, (name, r)  # not re-split
         else:
-            assert r["registers"] == 128, (name, r)
+            launch_regs = {2: 128, 1: 168}[nq]  # 65536 / threads, rounded down to a multiple of 8
+            assert r["registers"] == launch_regs, (name, r)
+    assert len(seen) == 28
 
 
 def test_backward_workspace_size_and_host_checks(lib):

@@ -15,8 +15,6 @@ import torch
 import tiled_attention_fwd_gb300 as fa
 from tiled_attention_fwd_gb300.inputs import Workload, as_f64_numpy, make_qkv
 
-from parity_util import TOL_BF16_L, TOL_BF16_O
-
 FAKE = 1 << 20  # aligned, non-null, never dereferenced by the host-side checks below
 
 
@@ -34,16 +32,24 @@ def _run(entry, w, q, k, v):
 
 @pytest.mark.gpu
 def test_noalloc_matches_fa_fwd_on_two_calls_in_a_row():
+    """fa_fwd_noalloc launches the same kernel as fa_fwd on the same inputs, so
+    each of two calls in a row must give identical bits.  The first two
+    workloads are small enough for the single-tile kernel; the third (160
+    heads, 480 two-tile work units) takes the two-tile kernel of the headline."""
     dev = torch.device("cuda", 0)
     workloads = [Workload("noalloc_a", 2, 3, 777, 128, "bf16", True, seed=21),
-                 Workload("noalloc_b", 1, 4, 300, 64, "bf16", False, seed=22)]
+                 Workload("noalloc_b", 1, 4, 300, 64, "bf16", False, seed=22),
+                 Workload("noalloc_c", 1, 160, 600, 128, "bf16", True, seed=23)]
     for w in workloads:
         q, k, v = (t.to(dev) for t in make_qkv(w))
         o_ref, l_ref = _run(fa.fa_fwd, w, q, k, v)
-        o, lse = _run(fa.fa_fwd_noalloc, w, q, k, v)
-        assert np.isfinite(o).all() and np.isfinite(lse).all(), w.name
-        assert np.abs(o - o_ref).max() <= TOL_BF16_O, w.name
-        assert np.abs(lse - l_ref).max() <= TOL_BF16_L, w.name
+        for call in range(2):
+            o, lse = _run(fa.fa_fwd_noalloc, w, q, k, v)
+            assert np.isfinite(o).all() and np.isfinite(lse).all(), (w.name, call)
+            assert np.array_equal(o, o_ref), (w.name, call, float(np.abs(o - o_ref).max()))
+            assert np.array_equal(lse, l_ref), (w.name, call, float(np.abs(lse - l_ref).max()))
+    # fa_status also reads (and clears) the no-alloc status word: no wait expired.
+    assert fa.fa_status(torch.cuda.current_stream(dev).cuda_stream) == 0
 
 
 def test_noalloc_rejects_bad_arguments_before_touching_a_device():

@@ -78,16 +78,6 @@ int current_device_state(DeviceState** out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int check_common(int B, int H, int N, int d, float scale) {
-  if (B < 1 || H < 1 || N < 1) return FA_ERR_BAD_SHAPE;
-  const long long bh = static_cast<long long>(B) * H;
-  if (bh > 0x7fffffffLL) return FA_ERR_BAD_SHAPE;
-  // Work units (B*H*ceil(N/256)) and launch-grid dimensions are 32-bit ints.
-  if (bh * ((static_cast<long long>(N) + 255) / 256) > 0x7fffffffLL) return FA_ERR_BAD_SHAPE;
-  if (static_cast<long long>(N) * (d > 0 ? d : 1) * 2 >= (1LL << 40)) return FA_ERR_BAD_SHAPE;
-  if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_BAD_SCALE;
-  return FA_OK;
-}
 
 LaunchCtx make_ctx(const DeviceState& s, void* stream) {
   LaunchCtx c;
@@ -121,6 +111,47 @@ int host_pipeline(DeviceState* s, HostPipeline** out) {
 }
 
 }  // namespace
+
+int check_common(int B, int H, int N, int d, float scale) {
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_BAD_SHAPE;
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh > 0x7fffffffLL) return FA_ERR_BAD_SHAPE;
+  // Work units (B*H*ceil(N/256)) and launch-grid dimensions are 32-bit ints.
+  if (bh * ((static_cast<long long>(N) + 255) / 256) > 0x7fffffffLL) return FA_ERR_BAD_SHAPE;
+  if (static_cast<long long>(N) * (d > 0 ? d : 1) * 2 >= (1LL << 40)) return FA_ERR_BAD_SHAPE;
+  if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_BAD_SCALE;
+  return FA_OK;
+}
+
+int check_fwd_bf16(const void* q, const void* k, const void* v, const void* o, const float* lse, int B, int H, int N,
+                   int d, float scale) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_NULL_POINTER;
+  const int rc = check_common(B, H, N, d, scale);
+  if (rc != FA_OK) return rc;
+  if (d != 32 && d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED_D;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return FA_ERR_MISALIGNED;
+  return FA_OK;
+}
+
+void contiguous_fwd_args(FwdArgs* a, const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                         int N, int d, float scale, int causal) {
+  a->q = q;
+  a->k = k;
+  a->v = v;
+  a->o = o;
+  a->lse = lse;
+  a->B = B;
+  a->H = H;
+  a->Nq = N;
+  a->Nk = N;
+  contiguous_strides(a->qs, H, N, d);
+  contiguous_strides(a->ks, H, N, d);
+  contiguous_strides(a->vs, H, N, d);
+  contiguous_strides(a->os, H, N, d);
+  a->scale = scale;
+  a->causal = causal != 0;
+}
 
 // Dispatch of the bf16 forward by head dimension; maps launch failures to FA_ERR_CUDA.
 int launch_tc(const FwdArgs& a, int d, const LaunchCtx& ctx) {
@@ -202,32 +233,13 @@ extern "C" {
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
            float scale, int causal, void* stream) {
-  if (!q || !k || !v || !o || !lse) return FA_ERR_NULL_POINTER;
-  int rc = fa::check_common(B, H, N, d, scale);
+  int rc = fa::check_fwd_bf16(q, k, v, o, lse, B, H, N, d, scale);
   if (rc != FA_OK) return rc;
-  if (d != 32 && d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED_D;
-  if (!fa::aligned16(q) || !fa::aligned16(k) || !fa::aligned16(v) || !fa::aligned16(o) ||
-      (reinterpret_cast<uintptr_t>(lse) & 3u))
-    return FA_ERR_MISALIGNED;
   fa::DeviceState* s = nullptr;
   rc = fa::current_device_state(&s);
   if (rc != FA_OK) return rc;
   fa::FwdArgs a;
-  a.q = q;
-  a.k = k;
-  a.v = v;
-  a.o = o;
-  a.lse = lse;
-  a.B = B;
-  a.H = H;
-  a.Nq = N;
-  a.Nk = N;
-  fa::contiguous_strides(a.qs, H, N, d);
-  fa::contiguous_strides(a.ks, H, N, d);
-  fa::contiguous_strides(a.vs, H, N, d);
-  fa::contiguous_strides(a.os, H, N, d);
-  a.scale = scale;
-  a.causal = causal != 0;
+  fa::contiguous_fwd_args(&a, q, k, v, o, lse, B, H, N, d, scale, causal);
   return fa::launch_tc(a, d, fa::make_ctx(*s, stream));
 }
 
@@ -467,11 +479,10 @@ int fa_status(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
   int word = 0;
   if (cudaMemcpy(&word, s->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
-  if (word != 0) {
-    if (cudaMemset(s->status, 0, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
-    return FA_ERR_TIMEOUT;
-  }
-  return FA_OK;
+  if (word != 0 && cudaMemset(s->status, 0, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+  const int na = fa::noalloc_take_status();
+  if (na == FA_ERR_CUDA) return FA_ERR_CUDA;
+  return (word != 0 || na == FA_ERR_TIMEOUT) ? FA_ERR_TIMEOUT : FA_OK;
 }
 
 int fa_selftest_wait(void* stream) {

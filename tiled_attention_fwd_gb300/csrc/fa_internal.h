@@ -122,6 +122,23 @@ int launch_bwd_strided_d64(const BwdArgs& a, const LaunchCtx& ctx);
 int launch_bwd_strided_d128(const BwdArgs& a, const LaunchCtx& ctx);
 int launch_bwd_strided_d256(const BwdArgs& a, const LaunchCtx& ctx);
 
+// Argument checks shared by the entry points (fa_api.cu); each returns FA_OK
+// or the FA_* code of the first violated rule.  check_common: B, H, N >= 1,
+// the index ranges, scale finite and > 0.  check_fwd_bf16: the pointers of
+// the contiguous bf16 forward (non-null, 16-byte aligned; lse 4-byte aligned),
+// check_common and a supported d.
+int check_common(int B, int H, int N, int d, float scale);
+int check_fwd_bf16(const void* q, const void* k, const void* v, const void* o, const float* lse, int B, int H, int N,
+                   int d, float scale);
+
+// Read and clear fa_fwd_noalloc's status word on the current device
+// (fa_noalloc.cu); FA_OK, FA_ERR_TIMEOUT or FA_ERR_CUDA.
+int noalloc_take_status();
+
+// Fill `a` for contiguous [B][H][N][d] tensors (N_q = N_k = N).
+void contiguous_fwd_args(FwdArgs* a, const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                         int N, int d, float scale, int causal);
+
 // The bf16 forward for d in {32, 64, 128, 256}; takes the contiguous kernels
 // when every tensor is contiguous [B][H][N][d], else the strided ones; returns
 // an FA_* code.  Defined in fa_api.cu.

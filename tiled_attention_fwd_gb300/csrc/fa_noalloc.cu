@@ -61,23 +61,36 @@ int noalloc_device(NoAllocDevice** out) {
 }
 
 }  // namespace
+
+// Read and clear the status word of the static scratch on the current device
+// (fa_status).  Synchronous copies to and from the symbol; allocates nothing.
+// Returns FA_OK (word was zero, or no fa_fwd_noalloc call was set up on this
+// device), FA_ERR_TIMEOUT (word was set; now cleared) or FA_ERR_CUDA.
+int noalloc_take_status() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lock(g_na_mutex);
+    if (!g_na_devices[dev].ready) return FA_OK;
+  }
+  int word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_noalloc_scratch, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+  if (word == 0) return FA_OK;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(g_noalloc_scratch, &zero, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+  return FA_ERR_TIMEOUT;
+}
+
 }  // namespace fa
 
 extern "C" int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                               int N, int d, float scale, int causal, void* stream) {
-  if (!q || !k || !v || !o || !lse) return FA_ERR_NULL_POINTER;
-  if (B < 1 || H < 1 || N < 1) return FA_ERR_BAD_SHAPE;
-  const long long bh = static_cast<long long>(B) * H;
-  if (bh > 0x7fffffffLL || bh * ((static_cast<long long>(N) + 255) / 256) > 0x7fffffffLL) return FA_ERR_BAD_SHAPE;
-  if (static_cast<long long>(N) * 256 * 2 >= (1LL << 40)) return FA_ERR_BAD_SHAPE;
-  if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_BAD_SCALE;
-  if (d != 32 && d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED_D;
-  const uintptr_t a16 = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
-                        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o);
-  if ((a16 & 15u) || (reinterpret_cast<uintptr_t>(lse) & 3u)) return FA_ERR_MISALIGNED;
+  // The same checks, in the same order, as fa_fwd.
+  int rc = fa::check_fwd_bf16(q, k, v, o, lse, B, H, N, d, scale);
+  if (rc != FA_OK) return rc;
   if (fa::kTcScratchWords > fa::kNoAllocScratchWords) return FA_ERR_SCRATCH;
   fa::NoAllocDevice* s = nullptr;
-  int rc = fa::noalloc_device(&s);
+  rc = fa::noalloc_device(&s);
   if (rc != FA_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // The status word must start at zero for this call; the array keeps whatever the previous call left.
@@ -88,20 +101,6 @@ extern "C" int fa_fwd_noalloc(const void* q, const void* k, const void* v, void*
   ctx.num_sms = s->num_sms;
   ctx.stream = st;
   fa::FwdArgs a;
-  a.q = q;
-  a.k = k;
-  a.v = v;
-  a.o = o;
-  a.lse = lse;
-  a.B = B;
-  a.H = H;
-  a.Nq = N;
-  a.Nk = N;
-  fa::contiguous_strides(a.qs, H, N, d);
-  fa::contiguous_strides(a.ks, H, N, d);
-  fa::contiguous_strides(a.vs, H, N, d);
-  fa::contiguous_strides(a.os, H, N, d);
-  a.scale = scale;
-  a.causal = causal != 0;
+  fa::contiguous_fwd_args(&a, q, k, v, o, lse, B, H, N, d, scale, causal);
   return fa::launch_tc(a, d, ctx);
 }

@@ -2,6 +2,7 @@
 // the per-head-dimension translation units fa_tc_d<D>.cu.
 #pragma once
 
+#include <atomic>
 #include <cmath>
 
 #include "fa_fwd_tc.cuh"
@@ -18,14 +19,18 @@ int launch_tc_impl(const FwdArgs& a, const LaunchCtx& ctx) {
     // (setmaxnreg); the split is sized for exactly LAUNCH_REGS per thread.  A
     // build with any other count would make setmaxnreg.inc wait forever, so it
     // is refused here.
-    static int checked_regs = -1;
-    if (checked_regs < 0) {
+    // Queried once per instantiation; concurrent first calls may both query
+    // (the same value), and the atomic keeps that free of a data race.
+    static std::atomic<int> checked_regs{-1};
+    int regs = checked_regs.load(std::memory_order_relaxed);
+    if (regs < 0) {
       cudaFuncAttributes attr;
       cudaError_t ea = cudaFuncGetAttributes(&attr, kernel);
       if (ea != cudaSuccess) return static_cast<int>(ea);
-      checked_regs = attr.numRegs;
+      regs = attr.numRegs;
+      checked_regs.store(regs, std::memory_order_relaxed);
     }
-    if (checked_regs != C::LAUNCH_REGS) return -2;
+    if (regs != C::LAUNCH_REGS) return -2;
   }
   // The attribute is per function and device; setting it again is cheap and idempotent.
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
