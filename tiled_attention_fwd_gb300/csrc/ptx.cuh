@@ -121,6 +121,18 @@ __device__ __forceinline__ void warp_arrive(uint32_t bar) {
   if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
+// The same arrival made by an elect.sync-chosen lane inside one asm block, so
+// the compiler sees no divergent branch (keeps register allocation of long
+// unrolled loops unchanged where the arrival sits in the middle of them).
+__device__ __forceinline__ void warp_arrive_elect(uint32_t bar) {
+  __syncwarp();
+  asm volatile(
+      "{\n\t.reg .pred PE;\n\t"
+      "elect.sync _|PE, 0xffffffff;\n\t"
+      "@PE mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(bar)
+      : "memory");
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
