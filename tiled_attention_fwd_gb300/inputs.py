@@ -28,7 +28,7 @@ class Workload:
     H: int
     N: int
     d: int
-    dtype: str  # "f32" or "bf16"
+    dtype: str  # "f32", "bf16" or "fp8" (e4m3 inputs with per-tensor factors, bf16 O)
     causal: bool
     seed: int
     qk_std: float = 1.0
@@ -46,17 +46,18 @@ class Workload:
 
     @property
     def torch_dtype(self) -> torch.dtype:
-        return torch.float32 if self.dtype == "f32" else torch.bfloat16
+        return {"f32": torch.float32, "bf16": torch.bfloat16, "fp8": torch.float8_e4m3fn}[self.dtype]
 
     @property
     def elem_bytes(self) -> int:
-        return 4 if self.dtype == "f32" else 2
+        return {"f32": 4, "bf16": 2, "fp8": 1}[self.dtype]
 
     @property
     def io_bytes(self) -> int:
-        """Bytes read (Q, K, V once) plus written (O once, L in fp32)."""
+        """Bytes read (Q, K, V once) plus written (O once, L in fp32); O is bf16 for fp8 inputs."""
         n = self.B * self.H * self.N * self.d
-        return 4 * n * self.elem_bytes + self.B * self.H * self.N * 4
+        o_bytes = 2 if self.dtype == "fp8" else self.elem_bytes
+        return 3 * n * self.elem_bytes + n * o_bytes + self.B * self.H * self.N * 4
 
     def with_(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
@@ -75,6 +76,9 @@ WORKLOADS = {
     "bf16_b2h16n8192d64_qk3": Workload("bf16_b2h16n8192d64_qk3", 2, 16, 8192, 64, "bf16", False, 4, 3.0),
     "bf16_b2h16n8192d128_qk3": Workload("bf16_b2h16n8192d128_qk3", 2, 16, 8192, 128, "bf16", False, 4, 3.0),
     "bf16_b2h16n8192d256_qk3": Workload("bf16_b2h16n8192d256_qk3", 2, 16, 8192, 256, "bf16", False, 4, 3.0),
+    # The low-precision variant on the headline shape and the d = 128 sweep point (e4m3 inputs).
+    "fp8_b4h16n4096d128_causal": Workload("fp8_b4h16n4096d128_causal", 4, 16, 4096, 128, "fp8", True, 2),
+    "fp8_b2h16n8192d128_qk3": Workload("fp8_b2h16n8192d128_qk3", 2, 16, 8192, 128, "fp8", False, 4, 3.0),
 }
 
 HEADLINE = "bf16_b4h16n4096d128_causal"
@@ -92,6 +96,36 @@ def make_qkv(w: Workload):
         k = k * w.qk_std
     dt = w.torch_dtype
     return q.to(dt).contiguous(), k.to(dt).contiguous(), v.to(dt).contiguous()
+
+
+E4M3_MAX = 448.0  # largest finite e4m3 value
+
+
+def make_qkv_fp8(w: Workload):
+    """Q, K, V of workload ``w`` quantised to e4m3 with one dequantisation
+    factor per tensor.
+
+    The same seeded fp32 draws as make_qkv (so the distributions are the
+    workload's); each tensor's factor is the power of two 2^ceil(log2(amax /
+    448)), which puts the largest magnitude just inside e4m3's range and keeps
+    every dequantised value (e4m3 value times factor) exact in fp32; the
+    tensor divided by its factor is rounded to e4m3 (nearest even).  Returns
+    ((q8, k8, v8) as torch.float8_e4m3fn CPU tensors, (q_descale, k_descale,
+    v_descale) as floats).
+    """
+    g = torch.Generator(device="cpu").manual_seed(w.seed)
+    shape = (w.B, w.H, w.N, w.d)
+    xs = [torch.randn(shape, generator=g, dtype=torch.float32) for _ in range(3)]
+    if w.qk_std != 1.0:
+        xs[0] = xs[0] * w.qk_std
+        xs[1] = xs[1] * w.qk_std
+    out, scales = [], []
+    for x in xs:
+        amax = float(x.abs().max())
+        f = 2.0 ** math.ceil(math.log2(amax / E4M3_MAX)) if amax > 0 else 1.0
+        out.append((x / f).to(torch.float8_e4m3fn).contiguous())
+        scales.append(f)
+    return tuple(out), tuple(scales)
 
 
 def make_dout(w: Workload):
