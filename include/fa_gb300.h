@@ -98,6 +98,33 @@ int fa_fwd_strided(const void* q, const void* k, const void* v, void* o, float* 
                    float scale, int causal, void* stream);
 
 /*
+ * fa_fwd_fp8 - the forward pass on e4m3 (fp8) inputs with bf16 output.
+ * Same computation as fa_fwd on the dequantised inputs: the pages define the
+ * method on real-valued inputs ("FlashAttention-2 from PyTorch to Triton",
+ * section "What We Are Building") and name low-precision attention only as a
+ * later variant ("Case Study: metal-flash-attention", closing section on MFA
+ * 2.0); the quantisation reading here is one fp32 dequantisation factor per
+ * tensor, real value = factor * e4m3 value.  S = Q8 K8^T runs on the tensor
+ * core in e4m3 with fp32 accumulation and is scaled by
+ * scale * q_descale * k_descale; the softmax is fa_fwd's (fp32 m and l); P is
+ * rounded to e4m3, V's dtype, before O += P V (the Triton kernel of the page
+ * above casts P to V's dtype); O = (P V) * v_descale / l is stored in bf16.
+ *
+ *   q, k, v   : device pointers to e4m3 (OCP E4M3FN, one byte each) [B][H][N][d],
+ *               contiguous, 16-byte aligned.
+ *   o         : device pointer to bf16 [B][H][N][d], 16-byte aligned.
+ *   lse       : device pointer to fp32 [B][H][N] (natural log of the dequantised logits).
+ *   d         : 64 or 128 (else FA_ERR_UNSUPPORTED_D).
+ *   scale     : softmax scale of the dequantised logits (the pages use 1/sqrt(d)).
+ *   q_descale, k_descale, v_descale : dequantisation factors, finite and > 0,
+ *               and scale * q_descale * k_descale finite (else FA_ERR_BAD_SCALE).
+ *   Other arguments, asynchrony, ownership and return codes as fa_fwd.
+ */
+int fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
+               int B, int H, int N, int d, float scale,
+               float q_descale, float k_descale, float v_descale, int causal, void* stream);
+
+/*
  * fa_fwd_f32 - fp32 forward pass on the CUDA cores (SIMT), all arithmetic in fp32.
  * Same computation as fa_fwd (the plain attention of "FlashAttention-2 from
  * PyTorch to Triton", section "What We Are Building").  Problems whose K and V

@@ -51,13 +51,19 @@ def weight_error(s: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
     return dp, p.sum(axis=1)
 
 
-def head_bounds(q, k, v, scale: float, causal: bool):
+def head_bounds(q, k, v, scale: float, causal: bool, row_block: int = 1024):
     """E (worst case) and sigma^2 (predicted variance of the P rounding) per
-    output element of one head; q, k, v are the dequantised fp64 inputs."""
-    s = oracle.scores(q, k, scale, causal)
-    dp, l = weight_error(s)
-    e = (dp @ np.abs(v)) / l[:, None]
-    sig2 = ((dp * dp) @ (v * v)) / (3.0 * (l * l)[:, None])
+    output element of one head; q, k, v are the dequantised fp64 inputs.
+    Rows are independent; they are taken in blocks to bound the memory."""
+    n = q.shape[0]
+    e = np.empty((n, v.shape[1]))
+    sig2 = np.empty((n, v.shape[1]))
+    av, v2 = np.abs(v), v * v
+    for a in range(0, n, row_block):
+        rows = np.arange(a, min(n, a + row_block))
+        dp, l = weight_error(oracle.scores(q, k, scale, causal, rows))
+        e[rows] = (dp @ av) / l[:, None]
+        sig2[rows] = ((dp * dp) @ v2) / (3.0 * (l * l)[:, None])
     return e, sig2
 
 

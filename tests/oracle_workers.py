@@ -5,6 +5,7 @@ from __future__ import annotations
 
 import numpy as np
 
+import fp8_util
 import oracle
 
 
@@ -36,3 +37,12 @@ def backward_head(args):
     b, h, q, k, v, do, o_gpu, scale, causal = args
     ref, mag = head_bounds(q, k, v, do, o_gpu, scale, causal)
     return b, h, ref, mag
+
+
+def fp8_head(args):
+    """(b, h, O, L, E, sigma^2) of one head of an e4m3 problem: the oracle on the
+    dequantised inputs and the per-element bounds of tests/fp8_util.py."""
+    b, h, q8, k8, v8, qd, kd, vd, scale, causal = args
+    o, lse = oracle.attention_fp8_head(q8, k8, v8, qd, kd, vd, scale, causal)
+    e, sig2 = fp8_util.head_bounds(q8 * qd, k8 * kd, v8 * vd, scale, causal)
+    return b, h, o, lse, e, sig2

@@ -102,33 +102,35 @@ def test_missing_library_fails_loudly(tmp_path):
 
 
 def test_tensor_core_kernels_fit_their_register_split():
-    """The two-tile d <= 128 kernels launch 512 threads at 128 registers and re-split them
+    """The two-tile d <= 128 kernels (bf16 and e4m3) launch 512 threads at 128 registers and re-split them
     (176 x 256 softmax + 160 x 128 correction and MMA/TMA, 80/80 or 72/88 = 65536); the
     single-tile d <= 128 kernels launch 384 threads at 168 (208 softmax, 152 correction,
     144 MMA/TMA); any other launch count would stall setmaxnreg, and none of them may spill."""
     if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
         pytest.skip("nvcc not available")
     files = {f"fa_tc_d{d}{s}.cu" for d in (32, 64, 128, 256) for s in ("", "_strided")}
+    files |= {f"fa_tc_fp8_d{d}.cu" for d in (64, 128)}
     rep = build.ptxas_report(files)
     tc = {k: v for k, v in rep.items() if "fa_fwd_tc_kernel" in k}
-    # 4 head dims x causal / not x contiguous / strided, plus the single-tile
-    # kernels of d = 32, 64, 128 (causal / not, contiguous / strided)
-    assert len(tc) == 28
-    # Template parameters <D, CAUSAL, STRIDED, NQ> in the mangled name.
-    pat = re.compile(r"fa_fwd_tc_kernelILi(\d+)ELb([01])ELb([01])ELi([12])E")
+    # bf16: 4 head dims x causal / not x contiguous / strided, plus the
+    # single-tile kernels of d = 32, 64, 128 (causal / not, contiguous /
+    # strided); e4m3: d = 64, 128 x causal / not x two-tile / single-tile.
+    assert len(tc) == 36
+    # Template parameters <D, CAUSAL, STRIDED, NQ, F8> in the mangled name.
+    pat = re.compile(r"fa_fwd_tc_kernelILi(\d+)ELb([01])ELb([01])ELi([12])ELb([01])E")
     seen = set()
     for name, r in tc.items():
         m = pat.search(name)
         assert m, f"unrecognised kernel name {name}"
         d, causal, strided, nq = int(m.group(1)), m.group(2), m.group(3), int(m.group(4))
-        seen.add((d, causal, strided, nq))
+        seen.add((d, causal, strided, nq, m.group(5)))
         assert r["spill_stores"] == 0 and r["spill_loads"] == 0, (name, r)
         if d == 256:
             assert nq == 1 and r["registers"] <= 168, (name, r)  # not re-split
         else:
             launch_regs = {2: 128, 1: 168}[nq]  # 65536 / threads, rounded down to a multiple of 8
             assert r["registers"] == launch_regs, (name, r)
-    assert len(seen) == 28
+    assert len(seen) == 36
 
 
 def test_backward_workspace_size_and_host_checks(lib):

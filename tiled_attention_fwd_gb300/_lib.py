@@ -22,6 +22,7 @@ _c_size_t = ctypes.c_size_t
 _SIGNATURES = {
     "fa_fwd": (_c_int, [_c_void_p] * 5 + [_c_int] * 4 + [_c_float, _c_int, _c_void_p]),
     "fa_fwd_f32": (_c_int, [_c_void_p] * 5 + [_c_int] * 4 + [_c_float, _c_int, _c_void_p]),
+    "fa_fwd_fp8": (_c_int, [_c_void_p] * 5 + [_c_int] * 4 + [_c_float] * 4 + [_c_int, _c_void_p]),
     "fa_fwd_strided": (_c_int, [_c_void_p] * 5 + [_c_int] * 5 + [_c_void_p] * 4 + [_c_float, _c_int, _c_void_p]),
     "fa_fwd_host_workspace_bytes": (_c_size_t, [_c_int] * 4),
     "fa_fwd_host": (_c_int, [_c_void_p] * 6 + [_c_size_t] + [_c_int] * 4 + [_c_float, _c_int, _c_void_p]),
@@ -107,6 +108,12 @@ def fa_fwd_strided(q, k, v, o, lse, B, H, Nq, Nk, d, q_stride, k_stride, v_strid
 def fa_fwd_f32(q, k, v, o, lse, B, H, N, d, scale, causal, stream) -> int:
     """fp32 SIMT forward; pointers are integers (device addresses)."""
     return load().fa_fwd_f32(q, k, v, o, lse, B, H, N, d, scale, int(bool(causal)), stream)
+
+
+def fa_fwd_fp8(q, k, v, o, lse, B, H, N, d, scale, q_descale, k_descale, v_descale, causal, stream) -> int:
+    """e4m3 tensor-core forward (bf16 O, fp32 L); pointers are integers (device addresses)."""
+    return load().fa_fwd_fp8(q, k, v, o, lse, B, H, N, d, scale, q_descale, k_descale, v_descale, int(bool(causal)),
+                             stream)
 
 
 def fa_fwd_host_workspace_bytes(B, H, N, d) -> int:
@@ -221,6 +228,36 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
                                 stream)
             name = "fa_fwd_strided"
     _check(rc, name)
+    return o, l
+
+
+def forward_fp8(q8, k8, v8, descales, causal: bool = False, scale: float | None = None, out=None, lse=None):
+    """O, L = attention forward of e4m3 CUDA tensors q8, k8, v8 [B, H, N, d]
+    (torch.float8_e4m3fn, contiguous, d in {64, 128}) whose real values are
+    descales[i] * x8 (one factor per tensor, in the order q, k, v).  Returns
+    (O, L): O bf16 [B, H, N, d] and L fp32 [B, H, N].  Enqueued on the
+    current stream."""
+    import torch
+
+    ts = (q8, k8, v8)
+    if any(t.dim() != 4 for t in ts) or not (q8.shape == k8.shape == v8.shape):
+        raise ValueError("q8, k8, v8 must be [B, H, N, d] of one shape")
+    if not all(t.is_cuda and t.dtype == torch.float8_e4m3fn and t.is_contiguous() for t in ts):
+        raise ValueError("q8, k8, v8 must be contiguous float8_e4m3fn CUDA tensors")
+    B, H, N, d = q8.shape
+    if scale is None:
+        scale = d ** -0.5
+    o = torch.empty(q8.shape, device=q8.device, dtype=torch.bfloat16) if out is None else out
+    if o.shape != q8.shape or o.dtype != torch.bfloat16 or not o.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor shaped like q8")
+    l = torch.empty((B, H, N), device=q8.device, dtype=torch.float32) if lse is None else lse
+    if l.shape != (B, H, N) or l.dtype != torch.float32 or not l.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor [B, H, N]")
+    qd, kd, vd = (float(x) for x in descales)
+    with torch.cuda.device(q8.device):
+        rc = fa_fwd_fp8(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), o.data_ptr(), l.data_ptr(), B, H, N, d,
+                        float(scale), qd, kd, vd, causal, _stream_handle(torch, q8.device))
+    _check(rc, "fa_fwd_fp8")
     return o, l
 
 

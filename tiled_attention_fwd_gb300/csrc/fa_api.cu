@@ -194,6 +194,20 @@ int encode_bf16_map(CUtensorMap* map, const void* ptr, int BH, int N, int D, int
   return r == CUDA_SUCCESS ? 0 : -1;
 }
 
+int encode_e4m3_map(CUtensorMap* map, const void* ptr, int BH, int N, int D, int box_cols, int box_rows,
+                    int swizzle_bytes) {
+  if (g_encode == nullptr) return -1;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N) * D};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapSwizzle swz = swizzle_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : -1;
+}
+
 int encode_bf16_map4(CUtensorMap* map, const void* ptr, int B, int H, int N, int D, const long long* stride,
                      int box_cols, int box_rows, int swizzle_bytes) {
   if (g_encode == nullptr) return -1;
@@ -241,6 +255,32 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   fa::FwdArgs a;
   fa::contiguous_fwd_args(&a, q, k, v, o, lse, B, H, N, d, scale, causal);
   return fa::launch_tc(a, d, fa::make_ctx(*s, stream));
+}
+
+int fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+               float scale, float q_descale, float k_descale, float v_descale, int causal, void* stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_NULL_POINTER;
+  int rc = fa::check_common(B, H, N, d, scale);
+  if (rc != FA_OK) return rc;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED_D;
+  const float f[3] = {q_descale, k_descale, v_descale};
+  for (float x : f)
+    if (!(std::isfinite(x) && x > 0.f)) return FA_ERR_BAD_SCALE;
+  if (!std::isfinite(scale * q_descale * k_descale) || !(scale * q_descale * k_descale > 0.f)) return FA_ERR_BAD_SCALE;
+  if (!fa::aligned16(q) || !fa::aligned16(k) || !fa::aligned16(v) || !fa::aligned16(o) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return FA_ERR_MISALIGNED;
+  fa::DeviceState* s = nullptr;
+  rc = fa::current_device_state(&s);
+  if (rc != FA_OK) return rc;
+  fa::FwdArgs a;
+  fa::contiguous_fwd_args(&a, q, k, v, o, lse, B, H, N, d, scale, causal);
+  a.q_descale = q_descale;
+  a.k_descale = k_descale;
+  a.v_descale = v_descale;
+  const fa::LaunchCtx ctx = fa::make_ctx(*s, stream);
+  const int e = d == 64 ? fa::launch_tc_fp8_d64(a, ctx) : fa::launch_tc_fp8_d128(a, ctx);
+  return e == 0 ? FA_OK : FA_ERR_CUDA;
 }
 
 int fa_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
@@ -507,7 +547,7 @@ const char* fa_strerror(int code) {
     case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA runtime or driver call failed";
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a bounded device-side wait expired";
     case FA_ERR_ARCH: return "FA_ERR_ARCH: the current device is not compute capability 10.3";
-    case FA_ERR_BAD_SCALE: return "FA_ERR_BAD_SCALE: scale must be finite and > 0";
+    case FA_ERR_BAD_SCALE: return "FA_ERR_BAD_SCALE: scale (and every dequantisation factor) must be finite and > 0";
     case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE: workspace too small";
     case FA_ERR_SCRATCH: return "FA_ERR_SCRATCH: the kernel needs more scratch than fa_fwd_noalloc's static array holds";
     default: return "unknown fa_gb300 error code";

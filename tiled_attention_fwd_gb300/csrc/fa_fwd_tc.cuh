@@ -57,7 +57,8 @@ struct TcParams {
   int n_kv;              // number of key tiles: ceil(N / BK)
   int n_qb;              // query blocks per head: ceil(N / (BQ * NQT))
   int total_units;       // BH * n_qb
-  float scale_log2;      // softmax scale * log2(e)
+  float scale_log2;      // softmax scale * log2(e) (e4m3 inputs: times the q and k dequantisation factors)
+  float o_scale;         // e4m3 inputs: the v dequantisation factor, applied with 1 / l (unused for bf16)
   float* lse;            // [BH][Nq], contiguous
   int* status;           // device status word
   unsigned long long limit_ns;  // time limit of each device-side wait
@@ -66,20 +67,27 @@ struct TcParams {
 // NQ: query tiles per work unit.  Two tiles (d <= 128) share every K/V tile;
 // one tile with double-buffered S serves d = 256 and, at d <= 128, problems
 // with too few 256-row units to occupy the SMs.
-template <int D, int NQ = (D <= 128 ? 2 : 1)>
+// F8: Q, K, V are e4m3 (one byte per element; tcgen05.mma kind::f8f6f4 with
+// K = 32 per instruction, P rounded to e4m3 and packed four to a TMEM column);
+// O is bf16 either way.
+template <int D, int NQ = (D <= 128 ? 2 : 1), bool F8 = false>
 struct TcCfg {
   static constexpr int BQ = 128;                       // query rows per tile (= TMEM lanes)
   static constexpr int NQT = NQ;                       // query tiles per work unit
+  static constexpr bool FP8 = F8;
+  static constexpr int EB = F8 ? 1 : 2;                // bytes per Q / K / V element
+  static constexpr int KM = 32 / EB;                   // K elements per MMA (32 bytes of an operand row)
   static constexpr int BK = (D <= 128) ? 128 : 64;     // keys per K/V tile
   static constexpr int LA = (NQT == 1) ? 2 : 1;        // K tiles needed before the first P V
-  static constexpr int SWB = (D * 2 >= 128) ? 128 : D * 2;  // swizzle span in bytes
+  static constexpr int SWB = (D * EB >= 128) ? 128 : D * EB;  // swizzle span in bytes
   static constexpr uint32_t SWZ = (SWB == 128) ? 2u : 4u;   // descriptor swizzle code
-  static constexpr int RC = SWB / 2;                   // bf16 columns per swizzle region
+  static constexpr int RC = SWB / EB;                  // elements per swizzle region
   static constexpr int NR = D / RC;                    // regions per tile row
   static constexpr int Q_REGION = BQ * SWB;
   static constexpr int KV_REGION = BK * SWB;
-  static constexpr int Q_TILE = BQ * D * 2;
-  static constexpr int KV_TILE = BK * D * 2;
+  static constexpr int Q_TILE = BQ * D * EB;
+  static constexpr int KV_TILE = BK * D * EB;
+  static constexpr int P_COLS_64 = 64 * EB / 4;        // TMEM columns holding P of 64 keys
   static constexpr int NO = NQT;                       // O accumulators in TMEM
   // Two-tile mode at d = 128 issues each P V product as two runs over the key
   // halves of P (64 keys each), the first as soon as the softmax has written
@@ -131,7 +139,7 @@ struct TcCfg {
   // Register split (d <= 128).  Two tiles, 512 threads launched at 128
   // registers each: softmax 176 and 160 between the correction and the
   // MMA/TMA warpgroups: 80 / 80, or 72 / 88 where that measured faster
-  // (contiguous d = 64; the strided epilogue needs the correction's 80);
+  // (contiguous bf16 d = 64; the strided and e4m3 epilogues need the correction's 80);
   // 2*128*176 + 128*160 = 65536.  One tile, 384 threads launched at 168:
   // softmax 208, correction 152, MMA/TMA 144; 128*(208 + 296) = 64512.
   // d = 256 (one tile, 64-column S) fits 168 everywhere and is not split.
@@ -139,12 +147,14 @@ struct TcCfg {
   static constexpr uint32_t REG_SOFTMAX = (NQT == 2) ? 176 : 208;
   static constexpr uint32_t REG_CORR_OTHER = (NQT == 2) ? 160 : 296;
   static constexpr __host__ __device__ uint32_t reg_corr(bool strided) {
-    return NQT == 1 ? 152 : ((!strided && D == 64) ? 72 : 80);
+    return NQT == 1 ? 152 : ((!strided && D == 64 && !F8) ? 72 : 80);
   }
   static constexpr int LAUNCH_REGS = 65536 / THREADS > 255 ? 255 : (65536 / THREADS) & ~7;
   static_assert(!SPLIT_REGS || NQT * 128 * REG_SOFTMAX + 128 * REG_CORR_OTHER <= THREADS * LAUNCH_REGS,
                 "register split exceeds the launch budget");
   static_assert(D == 32 || D == 64 || D == 128 || D == 256, "head dim");
+  static_assert(!F8 || D == 64 || D == 128, "e4m3 kernels: d = 64 or 128");
+  static_assert(SWB == 128 || SWB == 64, "swizzle span");
   static_assert(NQ == 1 || (NQ == 2 && D <= 128), "query tiles per unit");
   static_assert(NST >= 2, "K/V stages");
   static_assert(LA <= 2, "a stage holds at most two K tiles");
@@ -160,9 +170,9 @@ struct TcUnit {
   int nmax;
 };
 
-template <int D, bool CAUSAL, int NQ>
+template <int D, bool CAUSAL, int NQ, bool F8>
 __device__ __forceinline__ TcUnit tc_decode(int u, const TcParams& p) {
-  using C = TcCfg<D, NQ>;
+  using C = TcCfg<D, NQ, F8>;
   TcUnit w;
   const int qb = p.n_qb - 1 - u / p.BH;  // heaviest query blocks first
   w.bh = u % p.BH;
@@ -208,9 +218,9 @@ __device__ __forceinline__ bool wait_bar_drain(uint32_t bar, uint32_t parity, co
 }
 
 // Barrier addresses in shared memory.
-template <int D, int NQ>
+template <int D, int NQ, bool F8>
 struct TcBars {
-  using C = TcCfg<D, NQ>;
+  using C = TcCfg<D, NQ, F8>;
   uint32_t b0;
   // Q tile t loaded / free again (one phase per work unit).
   __device__ __forceinline__ uint32_t q_full(int t) const { return b0 + 8u * t; }
@@ -249,11 +259,11 @@ struct TcBars {
 // as soon as the current unit's last S_t product has completed (q_empty(t)).
 //
 // Single-tile mode: per unit, Q, then {K_0, K_1}, then {V_j, K_{j+2}}.
-template <int D, bool CAUSAL, bool STRIDED, int NQ>
+template <int D, bool CAUSAL, bool STRIDED, int NQ, bool F8>
 __device__ __forceinline__ void tc_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
-                                            const TcParams& p, const TcBars<D, NQ>& bar, uint32_t base,
+                                            const TcParams& p, const TcBars<D, NQ, F8>& bar, uint32_t base,
                                             const WaitGuard& g) {
-  using C = TcCfg<D, NQ>;
+  using C = TcCfg<D, NQ, F8>;
   const uint64_t pol_q = policy_evict_first();
   const uint64_t pol_kv = policy_evict_last();
   uint32_t pos = 0;       // stages issued so far
@@ -306,14 +316,14 @@ __device__ __forceinline__ void tc_producer(const CUtensorMap* tm_q, const CUten
     int uk = 0;
     int u = tc_unit(0);
     if (u < p.total_units) {
-      TcUnit w = tc_decode<D, CAUSAL, NQ>(u, p);
+      TcUnit w = tc_decode<D, CAUSAL, NQ, F8>(u, p);
       uint32_t s0, full;
       ok = load_q(w, 0) && stage_begin(1, s0, full);
       if (ok) load_tile(tm_k, s0, full, 0, w.bh);
       while (ok) {
         const int un = tc_unit(uk + 1);
         const bool has_next = un < p.total_units;
-        const TcUnit wn = tc_decode<D, CAUSAL, NQ>(has_next ? un : u, p);
+        const TcUnit wn = tc_decode<D, CAUSAL, NQ, F8>(has_next ? un : u, p);
         for (int j = 0; ok && j < w.nmax; ++j) {
           const bool k_here = j + 1 < w.nmax;
           const bool k_next = !k_here && has_next;
@@ -331,7 +341,7 @@ __device__ __forceinline__ void tc_producer(const CUtensorMap* tm_q, const CUten
     }
   } else {
     for (int uk = 0, u; ok && (u = tc_unit(uk)) < p.total_units; ++uk) {
-      const TcUnit w = tc_decode<D, CAUSAL, NQ>(u, p);
+      const TcUnit w = tc_decode<D, CAUSAL, NQ, F8>(u, p);
       if (!(ok = load_q(w, uk))) break;
       uint32_t s0, full;
       for (int t = -1; t < w.nmax; ++t) {
@@ -371,22 +381,24 @@ __device__ __forceinline__ void tc_producer(const CUtensorMap* tm_q, const CUten
 // Descriptors are kept as (low, high) words and built once: a tile position
 // or K step only adds a constant to the low word's address field (bits 0..13
 // hold address / 16, and no shared address reaches 2^18, so it never carries).
-template <int D, int NQ>
+template <int D, int NQ, bool F8>
 struct TcMma {
-  using C = TcCfg<D, NQ>;
-  static constexpr uint32_t IDESC_QK = make_idesc_bf16(128, C::BK, 0);
-  static constexpr uint32_t IDESC_PV = make_idesc_bf16(128, D, 1);
+  using C = TcCfg<D, NQ, F8>;
+  static constexpr uint32_t IDESC_QK = F8 ? make_idesc_e4m3(128, C::BK, 0) : make_idesc_bf16(128, C::BK, 0);
+  static constexpr uint32_t IDESC_PV = F8 ? make_idesc_e4m3(128, D, 1) : make_idesc_bf16(128, D, 1);
+  static constexpr int N_QK = D * C::EB / 32;      // MMAs per S = Q K^T (K = d)
+  static constexpr int N_PV = C::BK / C::KM;       // MMAs per P V (K = BK keys)
   // K-major (Q, K) and MN-major (V) operands share the stride byte offset
   // (8 rows of the swizzle span) and the swizzle mode.
   static constexpr uint32_t DESC_HI = sdesc_hi(8 * C::SWB, C::SWZ);
   // Address-field increments (16-byte units).
   static constexpr __host__ __device__ uint32_t q_step(int kk) {
-    return ((kk * 16 / C::RC) * C::Q_REGION + (kk * 16 % C::RC) * 2) >> 4;
+    return ((kk * C::KM / C::RC) * C::Q_REGION + (kk * C::KM % C::RC) * C::EB) >> 4;
   }
   static constexpr __host__ __device__ uint32_t k_step(int kk) {
-    return ((kk * 16 / C::RC) * C::KV_REGION + (kk * 16 % C::RC) * 2) >> 4;
+    return ((kk * C::KM / C::RC) * C::KV_REGION + (kk * C::KM % C::RC) * C::EB) >> 4;
   }
-  static constexpr __host__ __device__ uint32_t v_step(int kk) { return (kk * 16 * C::SWB) >> 4; }
+  static constexpr __host__ __device__ uint32_t v_step(int kk) { return (kk * C::KM * C::SWB) >> 4; }
   static constexpr uint32_t TILE_STEP = C::KV_TILE >> 4;
   static constexpr uint32_t QTILE_STEP = C::Q_TILE >> 4;
 
@@ -406,8 +418,8 @@ struct TcMma {
     static constexpr __host__ __device__ uint32_t db(int k) { return k_step(k) - k_step(k - 1); }
   };
   struct PvSteps {
-    static constexpr __host__ __device__ uint32_t ta(int) { return 8; }  // 16 bf16 = 8 TMEM columns
-    static constexpr __host__ __device__ uint32_t db(int) { return C::SWB; }
+    static constexpr __host__ __device__ uint32_t ta(int) { return 8; }  // KM elements of P = 8 TMEM columns
+    static constexpr __host__ __device__ uint32_t db(int) { return C::KM * C::SWB / 16; }  // KM rows of V
   };
   // S[buf] = Q[qt] K^T with K at tile position kpos; completion on s_full_bar.
   __device__ __forceinline__ void qk(int qt, int buf, uint32_t kpos, uint32_t s_full_bar) const {
@@ -416,12 +428,8 @@ struct TcMma {
     const uint32_t b = k_lo + kpos * TILE_STEP;
     // d <= 128: one block per product (measured faster at d = 32 and 64, equal
     // at d = 128); d = 256: one MMA per block (measured faster there).
-    if constexpr (D == 32) {
-      mma_ss_x2<QkSteps>(d_t, a, DESC_HI, b, DESC_HI, IDESC_QK, 0u);
-    } else if constexpr (D == 64) {
-      mma_ss_x4<QkSteps>(d_t, a, DESC_HI, b, DESC_HI, IDESC_QK, 0u);
-    } else if constexpr (D == 128) {
-      mma_ss_x8<QkSteps>(d_t, a, DESC_HI, b, DESC_HI, IDESC_QK, 0u);
+    if constexpr (D <= 128) {
+      mma_ss_run<N_QK, QkSteps, F8>(d_t, a, DESC_HI, b, DESC_HI, IDESC_QK, 0u);
     } else {
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
@@ -435,7 +443,7 @@ struct TcMma {
     const uint32_t a_t = tmem + C::TM_S + buf * C::TM_SB;
     const uint32_t b = v_lo + vpos * TILE_STEP;
     if constexpr (D <= 128) {
-      mma_ts_x8<PvSteps>(d_t, a_t, b, DESC_HI, IDESC_PV, acc ? 1u : 0u);
+      mma_ts_run<N_PV, PvSteps, F8>(d_t, a_t, b, DESC_HI, IDESC_PV, acc ? 1u : 0u);
     } else {
 #pragma unroll
       for (int kk = 0; kk < C::BK / 16; ++kk)
@@ -443,21 +451,21 @@ struct TcMma {
     }
   }
   // O[ot] (+)= P[buf][:, 64h .. 64h+63] V[64h .. 64h+63, :]: one key half of
-  // P V (BK = 128), 4 MMAs of K = 16; P's half h starts 32 TMEM columns in.
+  // P V (BK = 128); P's half h starts P_COLS_64 TMEM columns in, V's 64 rows in.
   __device__ __forceinline__ void pv_half(int ot, int buf, uint32_t vpos, int h, bool acc) const {
     const uint32_t d_t = tmem + C::TM_O + ot * D;
-    const uint32_t a_t = tmem + C::TM_S + buf * C::TM_SB + h * 32;
-    const uint32_t b = v_lo + vpos * TILE_STEP + h * 4 * C::SWB;
-    mma_ts_x4<PvSteps>(d_t, a_t, b, DESC_HI, IDESC_PV, acc ? 1u : 0u);
+    const uint32_t a_t = tmem + C::TM_S + buf * C::TM_SB + h * C::P_COLS_64;
+    const uint32_t b = v_lo + vpos * TILE_STEP + h * (64 * C::SWB / 16);
+    mma_ts_run<N_PV / 2, PvSteps, F8>(d_t, a_t, b, DESC_HI, IDESC_PV, acc ? 1u : 0u);
   }
   __device__ __forceinline__ void commit(uint32_t bar) const { mma_commit_elect(bar); }
 };
 
-template <int D, bool CAUSAL, int NQ>
-__device__ __forceinline__ void tc_mma(const TcParams& p, const TcBars<D, NQ>& bar, uint32_t base, uint32_t tmem,
+template <int D, bool CAUSAL, int NQ, bool F8>
+__device__ __forceinline__ void tc_mma(const TcParams& p, const TcBars<D, NQ, F8>& bar, uint32_t base, uint32_t tmem,
                                        const WaitGuard& g) {
-  using C = TcCfg<D, NQ>;
-  const TcMma<D, NQ> M(tmem, base);
+  using C = TcCfg<D, NQ, F8>;
+  const TcMma<D, NQ, F8> M(tmem, base);
   // Every lane waits (a non-blocking test first, then the bounded wait); the
   // outcome is made warp-uniform.
   auto wait = [&](uint32_t b, uint32_t par) -> bool {
@@ -532,14 +540,14 @@ __device__ __forceinline__ void tc_mma(const TcParams& p, const TcBars<D, NQ>& b
       return true;
     };
     if (u < p.total_units) {
-      TcUnit w = tc_decode<D, CAUSAL, NQ>(u, p);
+      TcUnit w = tc_decode<D, CAUSAL, NQ, F8>(u, p);
       uint32_t st;
       ok = stage_acquire(st) && first_qk(w, 0, 0, 2 * st) && first_qk(w, 0, 1, 2 * st);
       if (ok) M.commit(bar.kv_empty(st));
       while (ok) {
         const int un = tc_unit(uk + 1);
         const bool has_next = un < p.total_units;
-        const TcUnit wn = tc_decode<D, CAUSAL, NQ>(has_next ? un : u, p);
+        const TcUnit wn = tc_decode<D, CAUSAL, NQ, F8>(has_next ? un : u, p);
         for (int j = 0; ok && j < w.nmax; ++j) {
           if (!(ok = stage_acquire(st))) break;
           // In a unit's last step both P V products go first: the next unit's
@@ -561,7 +569,7 @@ __device__ __forceinline__ void tc_mma(const TcParams& p, const TcBars<D, NQ>& b
   } else {
     uint32_t qk_total = 0;  // S products issued so far
     for (int uk = 0, u; ok && (u = tc_unit(uk)) < p.total_units; ++uk) {
-      const TcUnit w = tc_decode<D, CAUSAL, NQ>(u, p);
+      const TcUnit w = tc_decode<D, CAUSAL, NQ, F8>(u, p);
       if (!(ok = wait(bar.q_full(0), uk & 1))) break;
       uint32_t st;
       if (!(ok = stage_acquire(st))) break;
@@ -605,10 +613,10 @@ __device__ __forceinline__ float ld_shared_volatile(const float* p) {
   return v;
 }
 
-template <int D, bool CAUSAL, int NQ>
-__device__ __forceinline__ void tc_softmax(const TcParams& p, const TcBars<D, NQ>& bar, uint8_t* gbase, uint32_t tmem,
+template <int D, bool CAUSAL, int NQ, bool F8>
+__device__ __forceinline__ void tc_softmax(const TcParams& p, const TcBars<D, NQ, F8>& bar, uint8_t* gbase, uint32_t tmem,
                                            int wg, int quarter, int lane, const WaitGuard& g) {
-  using C = TcCfg<D, NQ>;
+  using C = TcCfg<D, NQ, F8>;
   const int r = quarter * 32 + lane;  // row within the query tile = TMEM lane
   const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
   const int ot = (C::NQT == 2) ? wg : 0;
@@ -625,7 +633,7 @@ __device__ __forceinline__ void tc_softmax(const TcParams& p, const TcBars<D, NQ
   bool ok = true;
 
   for (int uk = 0, u; ok && (u = tc_unit(uk)) < p.total_units; ++uk) {
-    const TcUnit w = tc_decode<D, CAUSAL, NQ>(u, p);
+    const TcUnit w = tc_decode<D, CAUSAL, NQ, F8>(u, p);
     const int n = w.n[wg];
     if (n == 0) continue;
     const int row0 = w.row0 + wg * C::BQ;
@@ -701,20 +709,34 @@ __device__ __forceinline__ void tc_softmax(const TcParams& p, const TcBars<D, NQ
       uint64_t acc[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[i] = 0ull;  // (0.f, 0.f)
-      // P in chunks of 64 columns (32 bf16x2 words), each stored to TMEM as soon
-      // as it is packed.
+      // P in chunks of 64 columns (32 bf16x2 words, or 16 words of four e4m3),
+      // each stored to TMEM as soon as it is packed.
 #pragma unroll
       for (int h = 0; h < C::BK / 64; ++h) {
-        uint32_t pk[32];
+        if constexpr (C::FP8) {
+          uint32_t pk[16];
 #pragma unroll
-        for (int c = 64 * h; c < 64 * h + 64; c += 2) {
-          const float2 x = f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, nb2));
-          const float p0 = ex2(x.x);
-          const float p1 = ex2(x.y);
-          pk[(c >> 1) & 31] = pack_bf16x2(p0, p1);
-          acc[(c >> 1) & 3] = f2_add(acc[(c >> 1) & 3], f2_pack(p0, p1));
+          for (int c = 64 * h; c < 64 * h + 64; c += 4) {
+            const float2 x = f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, nb2));
+            const float2 y = f2_unpack(f2_fma(f2_pack(s[c + 2], s[c + 3]), sl2x2, nb2));
+            const float p0 = ex2(x.x), p1 = ex2(x.y), p2 = ex2(y.x), p3 = ex2(y.y);
+            pk[(c >> 2) & 15] = pack_e4m3x4(p0, p1, p2, p3);
+            acc[(c >> 1) & 3] = f2_add(acc[(c >> 1) & 3], f2_pack(p0, p1));
+            acc[((c >> 1) + 1) & 3] = f2_add(acc[((c >> 1) + 1) & 3], f2_pack(p2, p3));
+          }
+          tmem_st16(ts + h * C::P_COLS_64, pk);
+        } else {
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 64 * h; c < 64 * h + 64; c += 2) {
+            const float2 x = f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, nb2));
+            const float p0 = ex2(x.x);
+            const float p1 = ex2(x.y);
+            pk[(c >> 1) & 31] = pack_bf16x2(p0, p1);
+            acc[(c >> 1) & 3] = f2_add(acc[(c >> 1) & 3], f2_pack(p0, p1));
+          }
+          tmem_st32(ts + h * C::P_COLS_64, pk);
         }
-        tmem_st32(ts + h * 32, pk);
         if constexpr (C::PV_SPLIT) {
           if (h == 0) {  // first key half of P is in TMEM: its P V may start
             tmem_wait_st();
@@ -740,11 +762,11 @@ __device__ __forceinline__ void tc_softmax(const TcParams& p, const TcBars<D, NQ
 }
 
 // ------------------------------------------------------------------ correction + epilogue
-template <int D, bool CAUSAL, bool STRIDED, int NQ>
-__device__ __forceinline__ void tc_correction(const TcParams& p, const CUtensorMap* tm_o, const TcBars<D, NQ>& bar,
+template <int D, bool CAUSAL, bool STRIDED, int NQ, bool F8>
+__device__ __forceinline__ void tc_correction(const TcParams& p, const CUtensorMap* tm_o, const TcBars<D, NQ, F8>& bar,
                                               uint8_t* gbase, uint32_t tmem, int quarter, int lane,
                                               const WaitGuard& g) {
-  using C = TcCfg<D, NQ>;
+  using C = TcCfg<D, NQ, F8>;
   const int r = quarter * 32 + lane;
   const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
   const float* alpha_base = reinterpret_cast<const float*>(gbase + C::OFF_ALPHA);
@@ -829,7 +851,7 @@ __device__ __forceinline__ void tc_correction(const TcParams& p, const CUtensorM
     tc_fence_after();
     const float mrow = stat_m[su * 256 + t * 128 + r];
     const float lrow = stat_l[su * 256 + t * 128 + r];
-    const float inv_l = 1.f / lrow;
+    const float inv_l = (C::FP8 ? p.o_scale : 1.f) / lrow;
     const uint64_t il2 = f2_pack(inv_l, inv_l);
     const int row = w.row0 + t * C::BQ + r;
     const int wrow0 = w.row0 + t * C::BQ + quarter * 32;  // first row of this warp's box
@@ -879,7 +901,7 @@ __device__ __forceinline__ void tc_correction(const TcParams& p, const CUtensorM
   release_o(0);
   if (C::NO == 2) release_o(1);
   for (int uk = 0, u; ok && (u = tc_unit(uk)) < p.total_units; ++uk) {
-    const TcUnit w = tc_decode<D, CAUSAL, NQ>(u, p);
+    const TcUnit w = tc_decode<D, CAUSAL, NQ, F8>(u, p);
     // Same order as the MMA warp's P V products: (tile 0, j), (tile 1, j), (tile 0, j+1), ...
     for (int j = 0; ok && j < w.nmax; ++j) {
       if (ok && j >= 1 && j < w.n[0]) ok = rescale(0, a_cnt0, od0);
@@ -894,19 +916,19 @@ __device__ __forceinline__ void tc_correction(const TcParams& p, const CUtensorM
 }
 
 // ------------------------------------------------------------------ kernel
-template <int D, bool CAUSAL, bool STRIDED, int NQ>
-__global__ void __launch_bounds__(TcCfg<D, NQ>::THREADS, 1)
+template <int D, bool CAUSAL, bool STRIDED, int NQ, bool F8>
+__global__ void __launch_bounds__(TcCfg<D, NQ, F8>::THREADS, 1)
     fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                      const TcParams p) {
-  using C = TcCfg<D, NQ>;
+  using C = TcCfg<D, NQ, F8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const TcBars<D, NQ> bar{base + C::OFF_BAR};
+  const TcBars<D, NQ, F8> bar{base + C::OFF_BAR};
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::OFF_TMEM_SLOT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::OFF_ABORT);
 
@@ -951,14 +973,14 @@ __global__ void __launch_bounds__(TcCfg<D, NQ>::THREADS, 1)
 
   if (warp < C::SOFTMAX_WARPS) {
     if constexpr (C::SPLIT_REGS) regs_increase<C::REG_SOFTMAX>();
-    tc_softmax<D, CAUSAL, NQ>(p, bar, gbase, tmem, warp >> 2, warp & 3, lane, g);
+    tc_softmax<D, CAUSAL, NQ, F8>(p, bar, gbase, tmem, warp >> 2, warp & 3, lane, g);
   } else if (warp < C::SOFTMAX_WARPS + 4) {
     if constexpr (C::SPLIT_REGS) regs_decrease<C::reg_corr(STRIDED)>();
-    tc_correction<D, CAUSAL, STRIDED, NQ>(p, &tm_o, bar, gbase, tmem, warp & 3, lane, g);
+    tc_correction<D, CAUSAL, STRIDED, NQ, F8>(p, &tm_o, bar, gbase, tmem, warp & 3, lane, g);
   } else {
     if constexpr (C::SPLIT_REGS) regs_decrease<C::REG_CORR_OTHER - C::reg_corr(STRIDED)>();
-    if (warp == C::LOAD_WARP && lane == 0) tc_producer<D, CAUSAL, STRIDED, NQ>(&tm_q, &tm_k, &tm_v, p, bar, base, g);
-    if (warp == C::MMA_WARP) tc_mma<D, CAUSAL, NQ>(p, bar, base, tmem, g);
+    if (warp == C::LOAD_WARP && lane == 0) tc_producer<D, CAUSAL, STRIDED, NQ, F8>(&tm_q, &tm_k, &tm_v, p, bar, base, g);
+    if (warp == C::MMA_WARP) tc_mma<D, CAUSAL, NQ, F8>(p, bar, base, tmem, g);
   }
 
   __syncwarp();

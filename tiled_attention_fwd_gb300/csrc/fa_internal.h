@@ -38,6 +38,10 @@ struct FwdArgs {
   long long os[3];
   float scale;
   bool causal;
+  // e4m3 inputs only (fa_fwd_fp8): dequantisation factors, real x = factor * x8.
+  float q_descale = 1.f;
+  float k_descale = 1.f;
+  float v_descale = 1.f;
 };
 
 // Contiguous [B][H][N][d] strides.
@@ -60,6 +64,11 @@ int encode_bf16_map4(CUtensorMap* map, const void* ptr, int B, int H, int N, int
 int encode_bf16_map(CUtensorMap* map, const void* ptr, int BH, int N, int D, int box_cols, int box_rows,
                     int swizzle_bytes);
 
+// The same over a contiguous e4m3 [BH][N][D] tensor (one byte per element,
+// encoded as 8-bit unsigned data; TMA moves bytes).
+int encode_e4m3_map(CUtensorMap* map, const void* ptr, int BH, int N, int D, int box_cols, int box_rows,
+                    int swizzle_bytes);
+
 // Resolve the driver's tensor-map encoder (no device state, no allocation).  Returns 0 on success.
 int load_tensor_map_encoder();
 
@@ -76,6 +85,9 @@ int launch_tc_d32(const FwdArgs& a, const LaunchCtx& ctx);
 int launch_tc_d64(const FwdArgs& a, const LaunchCtx& ctx);
 int launch_tc_d128(const FwdArgs& a, const LaunchCtx& ctx);
 int launch_tc_d256(const FwdArgs& a, const LaunchCtx& ctx);
+// e4m3 Q, K, V, bf16 O (contiguous tensors).  Defined in fa_tc_fp8_d<D>.cu.
+int launch_tc_fp8_d64(const FwdArgs& a, const LaunchCtx& ctx);
+int launch_tc_fp8_d128(const FwdArgs& a, const LaunchCtx& ctx);
 // The same for strided tensors (4-D tensor maps).  Defined in fa_tc_d<D>_strided.cu.
 int launch_tc_strided_d32(const FwdArgs& a, const LaunchCtx& ctx);
 int launch_tc_strided_d64(const FwdArgs& a, const LaunchCtx& ctx);

@@ -10,10 +10,11 @@
 
 namespace fa {
 
-template <int D, bool CAUSAL, bool STRIDED, int NQ = TcCfg<D>::NQT>
+template <int D, bool CAUSAL, bool STRIDED, int NQ = TcCfg<D>::NQT, bool F8 = false>
 int launch_tc_impl(const FwdArgs& a, const LaunchCtx& ctx) {
-  using C = TcCfg<D, NQ>;
-  auto kernel = fa_fwd_tc_kernel<D, CAUSAL, STRIDED, NQ>;
+  using C = TcCfg<D, NQ, F8>;
+  static_assert(!(F8 && STRIDED), "e4m3 kernels take contiguous tensors");
+  auto kernel = fa_fwd_tc_kernel<D, CAUSAL, STRIDED, NQ, F8>;
   if constexpr (C::SPLIT_REGS) {
     // The warpgroups re-split the registers the block was launched with
     // (setmaxnreg); the split is sized for exactly LAUNCH_REGS per thread.  A
@@ -42,6 +43,12 @@ int launch_tc_impl(const FwdArgs& a, const LaunchCtx& ctx) {
     if (encode_bf16_map4(&mk, a.k, a.B, a.H, a.Nk, D, a.ks, C::RC, C::BK, C::SWB) != 0) return -1;
     if (encode_bf16_map4(&mv, a.v, a.B, a.H, a.Nk, D, a.vs, C::RC, C::BK, C::SWB) != 0) return -1;
     if (encode_bf16_map4(&mo, a.o, a.B, a.H, a.Nq, D, a.os, 32, 32, 64) != 0) return -1;
+  } else if constexpr (F8) {
+    // e4m3 Q, K, V as bytes; O is bf16 as in every other kernel.
+    if (encode_e4m3_map(&mq, a.q, a.B * a.H, a.Nq, D, C::RC, C::BQ, C::SWB) != 0) return -1;
+    if (encode_e4m3_map(&mk, a.k, a.B * a.H, a.Nk, D, C::RC, C::BK, C::SWB) != 0) return -1;
+    if (encode_e4m3_map(&mv, a.v, a.B * a.H, a.Nk, D, C::RC, C::BK, C::SWB) != 0) return -1;
+    if (encode_bf16_map(&mo, a.o, a.B * a.H, a.Nq, D, 32, 32, 64) != 0) return -1;
   } else {
     if (encode_bf16_map(&mq, a.q, a.B * a.H, a.Nq, D, C::RC, C::BQ, C::SWB) != 0) return -1;
     if (encode_bf16_map(&mk, a.k, a.B * a.H, a.Nk, D, C::RC, C::BK, C::SWB) != 0) return -1;
@@ -56,7 +63,14 @@ int launch_tc_impl(const FwdArgs& a, const LaunchCtx& ctx) {
   p.n_kv = (a.Nk + C::BK - 1) / C::BK;
   p.n_qb = (a.Nq + C::BQ * C::NQT - 1) / (C::BQ * C::NQT);
   p.total_units = p.BH * p.n_qb;
-  p.scale_log2 = a.scale * 1.4426950408889634f;
+  if constexpr (F8) {
+    // Logits of the dequantised inputs: (qf Q8)(kf K8)^T * scale.
+    p.scale_log2 = a.scale * a.q_descale * a.k_descale * 1.4426950408889634f;
+    p.o_scale = a.v_descale;
+  } else {
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.o_scale = 1.f;
+  }
   p.lse = a.lse;
   p.status = ctx.status;
   p.limit_ns = ctx.limit_ns;
@@ -73,13 +87,13 @@ namespace fa {
 // runs when even 128-row units would not outnumber the SMs: there the
 // two-tile kernel leaves most SMs idle and the one-tile chain per key tile is
 // shorter.
-template <int D, bool CAUSAL, bool STRIDED>
+template <int D, bool CAUSAL, bool STRIDED, bool F8 = false>
 int launch_tc_sized(const FwdArgs& a, const LaunchCtx& ctx) {
   if constexpr (D <= 128) {
     const long long units = static_cast<long long>(a.B) * a.H * ((a.Nq + 255) / 256);
-    if (2 * units <= ctx.num_sms) return launch_tc_impl<D, CAUSAL, STRIDED, 1>(a, ctx);
+    if (2 * units <= ctx.num_sms) return launch_tc_impl<D, CAUSAL, STRIDED, 1, F8>(a, ctx);
   }
-  return launch_tc_impl<D, CAUSAL, STRIDED>(a, ctx);
+  return launch_tc_impl<D, CAUSAL, STRIDED, TcCfg<D>::NQT, F8>(a, ctx);
 }
 
 }  // namespace fa
@@ -98,4 +112,12 @@ int launch_tc_sized(const FwdArgs& a, const LaunchCtx& ctx) {
   int launch_tc_strided_d##DIM(const FwdArgs& a, const LaunchCtx& ctx) {                             \
     return a.causal ? launch_tc_sized<DIM, true, true>(a, ctx) : launch_tc_sized<DIM, false, true>(a, ctx); \
   }                                                                                                  \
+  }
+
+// e4m3 Q, K, V (contiguous), bf16 O, in fa_tc_fp8_d<D>.cu.
+#define FA_DEFINE_TC_FP8_LAUNCHER(DIM)                                                                     \
+  namespace fa {                                                                                           \
+  int launch_tc_fp8_d##DIM(const FwdArgs& a, const LaunchCtx& ctx) {                                       \
+    return a.causal ? launch_tc_sized<DIM, true, false, true>(a, ctx) : launch_tc_sized<DIM, false, false, true>(a, ctx); \
+  }                                                                                                        \
   }

@@ -241,6 +241,19 @@ __host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, int b_mn_ma
          | (static_cast<uint32_t>(M >> 4) << 24);     // M / 16
 }
 
+// Instruction descriptor of tcgen05.mma kind::f8f6f4 with e4m3 A and B (format
+// code 0 in the A and B fields) and an fp32 accumulator; the other fields as
+// in make_idesc_bf16.
+__host__ __device__ constexpr uint32_t make_idesc_e4m3(int M, int N, int b_mn_major) {
+  return (1u << 4)                             // D format: f32
+         | (0u << 7)                           // A format: e4m3
+         | (0u << 10)                          // B format: e4m3
+         | (0u << 15)                          // A major: K
+         | (static_cast<uint32_t>(b_mn_major) << 16)  // B major
+         | (static_cast<uint32_t>(N >> 3) << 17)      // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);     // M / 16
+}
+
 // Shared-memory matrix descriptor (tcgen05 format), as two 32-bit words.
 // Low word: start address / 16 in bits 0..13, leading byte offset / 16 in
 // bits 16..29.  High word: stride byte offset / 16 in bits 0..13 (bits
@@ -503,24 +516,90 @@ __device__ __forceinline__ void mma_ts_x8(uint32_t d_tmem, uint32_t a_tmem, uint
       : "memory");
 }
 
-// Runs of N = 2, 4, 6 or 8 MMAs.
-template <int N, class S>
+// The same runs for kind::f8f6f4 (e4m3 operands, K = 32 per MMA: the same 32
+// bytes of each operand row as one kind::f16 MMA), lengths 2 and 4.
+#define FA_F8_SS_HEAD                                                       \
+  "{\n\t.reg .pred PE, PA, PT;\n\t.reg .b64 DA, DB;\n\t"                   \
+  "setp.ne.b32 PA, %6, 0;\n\tsetp.eq.b32 PT, 0, 0;\n\t"                     \
+  "mov.b64 DA, {%1, %2};\n\tmov.b64 DB, {%3, %4};\n\t"                      \
+  "elect.sync _|PE, 0xffffffff;\n\t"                                        \
+  "@PE tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], DA, DB, %5, PA;\n\t"
+#define FA_F8_SS_NEXT(IA, IB)                                               \
+  "add.s64 DA, DA, %" #IA ";\n\tadd.s64 DB, DB, %" #IB ";\n\t"              \
+  "@PE tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], DA, DB, %5, PT;\n\t"
+#define FA_F8_TS_HEAD                                                       \
+  "{\n\t.reg .pred PE, PA, PT;\n\t.reg .b64 DB;\n\t.reg .b32 TA;\n\t"      \
+  "setp.ne.b32 PA, %5, 0;\n\tsetp.eq.b32 PT, 0, 0;\n\t"                     \
+  "mov.b32 TA, %1;\n\tmov.b64 DB, {%2, %3};\n\t"                            \
+  "elect.sync _|PE, 0xffffffff;\n\t"                                        \
+  "@PE tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [TA], DB, %4, PA;\n\t"
+#define FA_F8_TS_NEXT(IA, IB)                                               \
+  "add.u32 TA, TA, %" #IA ";\n\tadd.s64 DB, DB, %" #IB ";\n\t"              \
+  "@PE tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [TA], DB, %4, PT;\n\t"
+
+template <class S>
+__device__ __forceinline__ void mma_ss_x2_f8(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
+                                              uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(FA_F8_SS_HEAD FA_F8_SS_NEXT(7, 8) "}"
+               ::"r"(d_tmem), "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate),
+               "n"(S::da(1)), "n"(S::db(1))
+               : "memory");
+}
+template <class S>
+__device__ __forceinline__ void mma_ss_x4_f8(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
+                                              uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(FA_F8_SS_HEAD FA_F8_SS_NEXT(7, 10) FA_F8_SS_NEXT(8, 11) FA_F8_SS_NEXT(9, 12) "}"
+               ::"r"(d_tmem), "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate),
+               "n"(S::da(1)), "n"(S::da(2)), "n"(S::da(3)), "n"(S::db(1)), "n"(S::db(2)), "n"(S::db(3))
+               : "memory");
+}
+template <class S>
+__device__ __forceinline__ void mma_ts_x2_f8(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(FA_F8_TS_HEAD FA_F8_TS_NEXT(6, 7) "}"
+               ::"r"(d_tmem), "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate), "n"(S::ta(1)),
+               "n"(S::db(1))
+               : "memory");
+}
+template <class S>
+__device__ __forceinline__ void mma_ts_x4_f8(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(FA_F8_TS_HEAD FA_F8_TS_NEXT(6, 9) FA_F8_TS_NEXT(7, 10) FA_F8_TS_NEXT(8, 11) "}"
+               ::"r"(d_tmem), "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate), "n"(S::ta(1)),
+               "n"(S::ta(2)), "n"(S::ta(3)), "n"(S::db(1)), "n"(S::db(2)), "n"(S::db(3))
+               : "memory");
+}
+
+// Runs of N = 2, 4, 6 or 8 MMAs (kind::f16), or N = 2 or 4 (kind::f8f6f4 when F8).
+template <int N, class S, bool F8 = false>
 __device__ __forceinline__ void mma_ss_run(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo, uint32_t b_hi,
                                            uint32_t idesc, uint32_t accumulate) {
-  static_assert(N == 2 || N == 4 || N == 6 || N == 8, "run length");
-  if constexpr (N == 2) mma_ss_x2<S>(d_tmem, a_lo, a_hi, b_lo, b_hi, idesc, accumulate);
-  if constexpr (N == 4) mma_ss_x4<S>(d_tmem, a_lo, a_hi, b_lo, b_hi, idesc, accumulate);
-  if constexpr (N == 6) mma_ss_x6<S>(d_tmem, a_lo, a_hi, b_lo, b_hi, idesc, accumulate);
-  if constexpr (N == 8) mma_ss_x8<S>(d_tmem, a_lo, a_hi, b_lo, b_hi, idesc, accumulate);
+  if constexpr (F8) {
+    static_assert(N == 2 || N == 4, "run length");
+    if constexpr (N == 2) mma_ss_x2_f8<S>(d_tmem, a_lo, a_hi, b_lo, b_hi, idesc, accumulate);
+    if constexpr (N == 4) mma_ss_x4_f8<S>(d_tmem, a_lo, a_hi, b_lo, b_hi, idesc, accumulate);
+  } else {
+    static_assert(N == 2 || N == 4 || N == 6 || N == 8, "run length");
+    if constexpr (N == 2) mma_ss_x2<S>(d_tmem, a_lo, a_hi, b_lo, b_hi, idesc, accumulate);
+    if constexpr (N == 4) mma_ss_x4<S>(d_tmem, a_lo, a_hi, b_lo, b_hi, idesc, accumulate);
+    if constexpr (N == 6) mma_ss_x6<S>(d_tmem, a_lo, a_hi, b_lo, b_hi, idesc, accumulate);
+    if constexpr (N == 8) mma_ss_x8<S>(d_tmem, a_lo, a_hi, b_lo, b_hi, idesc, accumulate);
+  }
 }
-template <int N, class S>
+template <int N, class S, bool F8 = false>
 __device__ __forceinline__ void mma_ts_run(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
                                            uint32_t idesc, uint32_t accumulate) {
-  static_assert(N == 2 || N == 4 || N == 6 || N == 8, "run length");
-  if constexpr (N == 2) mma_ts_x2<S>(d_tmem, a_tmem, b_lo, b_hi, idesc, accumulate);
-  if constexpr (N == 4) mma_ts_x4<S>(d_tmem, a_tmem, b_lo, b_hi, idesc, accumulate);
-  if constexpr (N == 6) mma_ts_x6<S>(d_tmem, a_tmem, b_lo, b_hi, idesc, accumulate);
-  if constexpr (N == 8) mma_ts_x8<S>(d_tmem, a_tmem, b_lo, b_hi, idesc, accumulate);
+  if constexpr (F8) {
+    static_assert(N == 2 || N == 4, "run length");
+    if constexpr (N == 2) mma_ts_x2_f8<S>(d_tmem, a_tmem, b_lo, b_hi, idesc, accumulate);
+    if constexpr (N == 4) mma_ts_x4_f8<S>(d_tmem, a_tmem, b_lo, b_hi, idesc, accumulate);
+  } else {
+    static_assert(N == 2 || N == 4 || N == 6 || N == 8, "run length");
+    if constexpr (N == 2) mma_ts_x2<S>(d_tmem, a_tmem, b_lo, b_hi, idesc, accumulate);
+    if constexpr (N == 4) mma_ts_x4<S>(d_tmem, a_tmem, b_lo, b_hi, idesc, accumulate);
+    if constexpr (N == 6) mma_ts_x6<S>(d_tmem, a_tmem, b_lo, b_hi, idesc, accumulate);
+    if constexpr (N == 8) mma_ts_x8<S>(d_tmem, a_tmem, b_lo, b_hi, idesc, accumulate);
+  }
 }
 
 // Arrive once on `bar` when every tcgen05 operation the warp issued so far
@@ -643,6 +722,20 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Four fp32 values to four e4m3 bytes (round to nearest even, saturating to
+// +-448); `p0` in bits 0..7 (the lowest K index first, as a TMEM A operand of
+// kind::f8f6f4 holds four consecutive K elements per 32-bit column).
+__device__ __forceinline__ uint32_t pack_e4m3x4(float p0, float p1, float p2, float p3) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r)
+      : "f"(p0), "f"(p1), "f"(p2), "f"(p3));
   return r;
 }
 
