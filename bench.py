@@ -43,6 +43,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "FA2 fwd TFLOP/s, bf16 B4 H16 N4096 d128 causal; % of GB300 dense peak"
+FP8_METRIC = "FA2 fwd TFLOP/s, fp8 (e4m3) inputs, bf16 output; % of GB300 dense fp8 peak"
+FP8_OVER_BF16 = 2.0  # nominal dense fp8 / bf16 tensor rate (4.5 / 2.25 PFLOP/s)
 BWD_METRIC = "FA2 bwd TFLOP/s (2.5x the forward's algorithmic FLOPs), bf16; % of GB300 dense peak"
 BWD_FLOP_FACTOR = 2.5  # dV = P^T dO, dP = dO V^T, dQ = dS K, dK = dS^T Q, plus S = Q K^T recomputed
 UNIT = "TFLOP/s"
@@ -278,17 +280,33 @@ def make_pool(cores: int):
     return ctx.Pool(cores)
 
 
+def workload_inputs(w):
+    """Host inputs of workload w: (q, k, v) in its dtype, plus the three
+    dequantisation factors for e4m3 workloads (None otherwise)."""
+    from tiled_attention_fwd_gb300.inputs import make_qkv, make_qkv_fp8
+
+    if w.dtype == "fp8":
+        return make_qkv_fp8(w)
+    return make_qkv(w), None
+
+
+def oracle_inputs(w, qkv, factors):
+    """The real-valued inputs the oracle takes: e4m3 values times their factors
+    (exact in fp32 for the power-of-two factors of the synthetic inputs)."""
+    if factors is None:
+        return qkv
+    return tuple(x.float() * f for x, f in zip(qkv, factors))
+
+
 # ------------------------------------------------------------------ reference arm
 def run_reference(args, w):
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if rank != 0:
         return 0
-    from tiled_attention_fwd_gb300.inputs import make_qkv
-
     cores = os.cpu_count() or 1
     pool = make_pool(cores)
-    inputs = make_qkv(w)
+    inputs = oracle_inputs(w, *workload_inputs(w))
     bwd = args.pass_ == "bwd"
     budget = max(2.0, 60.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
@@ -305,7 +323,8 @@ def run_reference(args, w):
               f"processes (one head each, fp64 {'backward' if bwd else 'forward'}, BLAS single-threaded); "
               f"{heads} heads in {args.steps} steps")
     line = {
-        "impl": "reference", "metric": BWD_METRIC if bwd else METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "impl": "reference", "metric": BWD_METRIC if bwd else (FP8_METRIC if w.dtype == "fp8" else METRIC),
+        "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": secs / max(1, args.steps) * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -318,8 +337,11 @@ def run_reference(args, w):
 
 
 def config_of(w):
+    inputs = f"seeded iid normal (seed {w.seed}, Q/K std {w.qk_std})"
+    if w.dtype == "fp8":
+        inputs += ", quantised to e4m3 with one power-of-two factor per tensor; O bf16"
     return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
-            "dtype": w.dtype, "inputs": f"seeded iid normal (seed {w.seed}, Q/K std {w.qk_std})",
+            "dtype": w.dtype, "inputs": inputs,
             "l2": "flushed (256 MB write) between timed steps", "layout": "[B,H,N,d] contiguous"}
 
 
@@ -329,7 +351,6 @@ def run_ours(args, w):
     import torch.distributed as dist
 
     import tiled_attention_fwd_gb300 as fa
-    from tiled_attention_fwd_gb300.inputs import make_qkv
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -350,18 +371,19 @@ def run_ours(args, w):
             dist.barrier()
         torch.cuda.synchronize()
 
-    q, k, v = make_qkv(w)
+    (q, k, v), factors = workload_inputs(w)
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
-    o = torch.empty_like(qd)
+    o = torch.empty(q.shape, device=dev, dtype=torch.bfloat16 if w.dtype == "fp8" else q.dtype)
     lse = torch.empty((w.B, w.H, w.N), device=dev, dtype=torch.float32)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
-    fn = fa.fa_fwd if w.dtype == "bf16" else fa.fa_fwd_f32
+    fn = {"bf16": fa.fa_fwd, "f32": fa.fa_fwd_f32, "fp8": fa.fa_fwd_fp8}[w.dtype]
+    extra = tuple(factors) if factors is not None else ()
 
     def step():
         rc = fn(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), lse.data_ptr(), w.B, w.H, w.N, w.d,
-                w.scale, w.causal, sh)
+                w.scale, *extra, w.causal, sh)
         if rc != 0:
             raise fa.FAError(rc, fn.__name__)
 
@@ -432,10 +454,42 @@ def run_ours(args, w):
                "h2d_bytes_per_step": 3 * tb, "d2h_bytes_per_step": tb + w.B * w.H * w.N * 4,
                "ms_per_step": e2e_s / args.steps * 1e3, "api": "fa_fwd_host (C ABI, pinned host buffers)"}
         fa.check_status(dev)
+    if not args.no_e2e and w.dtype == "fp8":
+        # e4m3 inputs: the public Python API on pinned host tensors (H2D of the
+        # three e4m3 tensors, fa_fwd_fp8, D2H of O and L), every step.
+        hq, hk, hv = (t.pin_memory() for t in (q, k, v))
+        ho = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+        hl = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
+        dq8, dk8, dv8 = (torch.empty_like(qd) for _ in range(3))
+
+        def host_step():
+            for src, dst in zip((hq, hk, hv), (dq8, dk8, dv8)):
+                dst.copy_(src, non_blocking=True)
+            fa.forward_fp8(dq8, dk8, dv8, factors, causal=w.causal, scale=w.scale, out=o, lse=lse)
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            host_step()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            host_step()
+        e1.record(stream)
+        barrier()
+        e2e_s = aggregate_ranks(e0.elapsed_time(e1) / 1e3, world, reduce_max)
+        n = w.B * w.H * w.N * w.d
+        e2e = {"value": job_throughput(world, args.steps, w.flops, e2e_s), "unit": UNIT,
+               "h2d_bytes_per_step": 3 * n, "d2h_bytes_per_step": 2 * n + w.B * w.H * w.N * 4,
+               "ms_per_step": e2e_s / args.steps * 1e3,
+               "api": "tiled_attention_fwd_gb300.forward_fp8 (pinned host tensors, copies on the stream)"}
+        fa.check_status(dev)
 
     cpu = None
     if want_cpu:
-        tflops, heads, secs = oracle_sample(w, args.cpu_seconds, pool, cores, (q, k, v))
+        tflops, heads, secs = oracle_sample(w, args.cpu_seconds, pool, cores, oracle_inputs(w, (q, k, v), factors))
         cpu = {"value": tflops, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"{heads} whole heads of the workload (fp64 standard attention, one head per worker "
                          f"process, {cores} processes, BLAS single-threaded) in {secs:.1f} s"}
@@ -443,18 +497,23 @@ def run_ours(args, w):
         pool.close()
 
     peaks, src = load_peaks()
-    peak = peaks["bf16_tflops"]
+    peak = peaks["bf16_tflops"] * (FP8_OVER_BF16 if w.dtype == "fp8" else 1.0)
     achieved = w.flops / (kernel_ms / 1e3) / 1e12
     clock_rec = clocks.summary()
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     exps = exp_rate(w, kernel_ms, sms, clock_rec.get("sm_mhz"))
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-            "traffic": load_traffic(w.name), "peak_source": f"bf16 dense burst, {src}",
-            "kernel": f"fa_fwd_tc_kernel<{w.d},{str(w.causal).lower()}>" if w.dtype == "bf16" else "fa_fwd_simt_kernel",
+            "traffic": load_traffic(w.name),
+            "peak_source": (f"fp8 dense = bf16 dense burst ({src}) x {FP8_OVER_BF16:g}, the nominal fp8/bf16 ratio"
+                            if w.dtype == "fp8" else f"bf16 dense burst, {src}"),
+            "kernel": {"bf16": f"fa_fwd_tc_kernel<{w.d},{str(w.causal).lower()}>",
+                       "fp8": f"fa_fwd_tc_kernel<{w.d},{str(w.causal).lower()},e4m3>",
+                       "f32": "fa_fwd_simt_kernel"}[w.dtype],
             "flops_per_launch": w.flops}
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "metric": FP8_METRIC if w.dtype == "fp8" else METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_s / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
             "config": config_of(w), "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
@@ -628,6 +687,7 @@ REPORT_WORKLOADS = [
     "f32_b1h1n128d16", "f32_b1h1n128d16_causal", "bf16_b8h1n1024d64", "bf16_b8h1n1024d64_causal",
     "bf16_b4h16n4096d128_causal", "bf16_b1h32n16384d128_causal", "bf16_b2h16n8192d32_qk3",
     "bf16_b2h16n8192d64_qk3", "bf16_b2h16n8192d128_qk3", "bf16_b2h16n8192d256_qk3",
+    "fp8_b4h16n4096d128_causal", "fp8_b2h16n8192d128_qk3",
 ]
 
 
@@ -639,8 +699,8 @@ def run_report(args):
     so the full config's oracle time is that rate scaled to all heads)."""
     import torch
 
-    from tiled_attention_fwd_gb300 import check_status, fa_fwd, fa_fwd_f32
-    from tiled_attention_fwd_gb300.inputs import WORKLOADS, make_qkv
+    from tiled_attention_fwd_gb300 import check_status, fa_fwd, fa_fwd_f32, fa_fwd_fp8
+    from tiled_attention_fwd_gb300.inputs import WORKLOADS
 
     cores = os.cpu_count() or 1
     pool = make_pool(cores)  # spawned before the first GPU call
@@ -653,14 +713,15 @@ def run_report(args):
     rows = []
     for name in REPORT_WORKLOADS:
         w = WORKLOADS[name]
-        host = make_qkv(w)
+        host, factors = workload_inputs(w)
         q, k, v = (t.to(dev) for t in host)
-        o = torch.empty_like(q)
+        o = torch.empty(q.shape, device=dev, dtype=torch.bfloat16 if w.dtype == "fp8" else q.dtype)
         lse = torch.empty(q.shape[:-1], device=dev, dtype=torch.float32)
 
-        fn = fa_fwd if w.dtype == "bf16" else fa_fwd_f32
+        fn = {"bf16": fa_fwd, "f32": fa_fwd_f32, "fp8": fa_fwd_fp8}[w.dtype]
+        extra = tuple(float(f) for f in factors) if factors is not None else ()
         call = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), w.B, w.H, w.N, w.d,
-                float(w.scale), int(w.causal), torch.cuda.current_stream(dev).cuda_stream)
+                float(w.scale), *extra, int(w.causal), torch.cuda.current_stream(dev).cuda_stream)
 
         def launch():  # the C ABI directly, so that no host work sits between the events
             rc = fn(*call)
@@ -685,10 +746,12 @@ def run_report(args):
         med = statistics.median(times)
         tflops = w.flops / (med * 1e-3) / 1e12
         exps = exp_rate(w, med, torch.cuda.get_device_properties(dev).multi_processor_count, None)
-        ora, heads, secs = oracle_sample(w, args.report_cpu_seconds, pool, cores, host)
+        ora, heads, secs = oracle_sample(w, args.report_cpu_seconds, pool, cores, oracle_inputs(w, host, factors))
+        own_peak = peak * (FP8_OVER_BF16 if w.dtype == "fp8" else 1.0)
         row = {"workload": name, "dtype": w.dtype, "causal": w.causal, "gflop": w.flops / 1e9,
                "gpu_ms_median": med, "gpu_ms_min": min(times), "gpu_ms_max": max(times), "runs": runs,
-               "tflops": tflops, "frac_of_bf16_peak": tflops / peak, "peak_tflops": peak, "peak_source": peak_src,
+               "tflops": tflops, "frac_of_bf16_peak": tflops / peak, "frac_of_own_peak": tflops / own_peak,
+               "peak_tflops": own_peak, "peak_source": peak_src,
                "exp_per_s": exps["per_s"], "exp_frac_of_mufu": exps["frac"],
                "oracle_tflops": ora, "oracle_heads": heads, "oracle_s": secs,
                "oracle_full_s": w.flops / (ora * 1e12), "oracle_cores": cores}
@@ -696,11 +759,13 @@ def run_report(args):
         print(json.dumps(row), flush=True)
     pool.close()
     print(f"\n| config | GFLOP | GPU median / min / max (ms, {runs} runs) | TFLOP/s | of bf16 peak | "
-          f"exp/s (of MUFU at 2070 MHz) | CPU oracle ({cores} cores): TFLOP/s | oracle s, full config |")
-    print("|---|---|---|---|---|---|---|---|")
+          f"of own dtype's peak | exp/s (of MUFU at 2070 MHz) | CPU oracle ({cores} cores): TFLOP/s | "
+          f"oracle s, full config |")
+    print("|---|---|---|---|---|---|---|---|---|")
     for r in rows:
         print(f"| `{r['workload']}` | {r['gflop']:.3g} | {r['gpu_ms_median']:.4f} / {r['gpu_ms_min']:.4f} / "
               f"{r['gpu_ms_max']:.4f} | {r['tflops']:.4g} | {r['frac_of_bf16_peak']:.3g} | "
+              f"{r['frac_of_own_peak']:.3g} | "
               f"{r['exp_per_s']:.3g} ({r['exp_frac_of_mufu']:.3g}) | "
               f"{r['oracle_tflops']:.3g} | {r['oracle_full_s']:.3g} |")
     return 0
@@ -723,7 +788,7 @@ def main(argv=None):
     ap.add_argument("--report", action="store_true",
                     help="time the forward on every config beside the CPU oracle and print a table")
     ap.add_argument("--report-cpu-seconds", type=float, default=8.0, help="CPU oracle budget per config in --report")
-    ap.add_argument("--clock-soak-s", type=float, default=0.6,
+    ap.add_argument("--clock-soak-s", type=float, default=0.3,
                     help="seconds of identical untimed load before the timed steps (a quarter of it after), "
                          "so that the clock samples bracket the timed region")
     args = ap.parse_args(argv)
