@@ -116,8 +116,8 @@ def test_tensor_core_kernels_fit_their_register_split():
     # single-tile kernels of d = 32, 64, 128 (causal / not, contiguous /
     # strided); e4m3: d = 64, 128 x causal / not x two-tile / single-tile.
     assert len(tc) == 36
-    # Template parameters <D, CAUSAL, STRIDED, NQ, F8> in the mangled name.
-    pat = re.compile(r"fa_fwd_tc_kernelILi(\d+)ELb([01])ELb([01])ELi([12])ELb([01])E")
+    # Template parameters <D, CAUSAL, STRIDED, NQ, VAR> in the mangled name.
+    pat = re.compile(r"fa_fwd_tc_kernelILi(\d+)ELb([01])ELb([01])ELi([12])ELi([012])E")
     seen = set()
     for name, r in tc.items():
         m = pat.search(name)

@@ -49,6 +49,9 @@
 
 namespace fa {
 
+// Kernel variants (template parameter VAR).
+enum : int { kVarBf16 = 0, kVarE4m3 = 1, kVarPair = 2 };
+
 struct TcParams {
   int Nq;                // query rows per head
   int Nk;                // key / value rows per head
@@ -67,26 +70,35 @@ struct TcParams {
 // NQ: query tiles per work unit.  Two tiles (d <= 128) share every K/V tile;
 // one tile with double-buffered S serves d = 256 and, at d <= 128, problems
 // with too few 256-row units to occupy the SMs.
-// F8: Q, K, V are e4m3 (one byte per element; tcgen05.mma kind::f8f6f4 with
-// K = 32 per instruction, P rounded to e4m3 and packed four to a TMEM column);
-// O is bf16 either way.
-template <int D, int NQ = (D <= 128 ? 2 : 1), bool F8 = false>
+// VAR: kVarBf16 (bf16 Q, K, V); kVarE4m3: Q, K, V are e4m3 (one byte per
+// element; tcgen05.mma kind::f8f6f4 with K = 32 per instruction, P rounded to
+// e4m3 and packed four to a TMEM column; O is bf16 either way); kVarPair:
+// bf16 at d = 256 on CTA pairs (cta_group::2, M = 256, BK = 128).
+template <int D, int NQ = (D <= 128 ? 2 : 1), int VAR = kVarBf16>
 struct TcCfg {
   static constexpr int BQ = 128;                       // query rows per tile (= TMEM lanes)
   static constexpr int NQT = NQ;                       // query tiles per work unit
-  static constexpr bool FP8 = F8;
-  static constexpr int EB = F8 ? 1 : 2;                // bytes per Q / K / V element
+  static constexpr bool FP8 = (VAR == kVarE4m3);
+  static constexpr bool PAIR = (VAR == kVarPair);
+  static constexpr int EB = FP8 ? 1 : 2;                // bytes per Q / K / V element
   static constexpr int KM = 32 / EB;                   // K elements per MMA (32 bytes of an operand row)
-  static constexpr int BK = (D <= 128) ? 128 : 64;     // keys per K/V tile
+  static constexpr int BK = (D <= 128 || PAIR) ? 128 : 64;  // keys per K/V tile
+  // Query tiles of a work unit (256 rows for a CTA pair: one tile per CTA).
+  static constexpr int UNIT_TILES = PAIR ? 2 : NQT;
+  // A CTA pair holds half of every K tile (BK / 2 keys) and half of every V
+  // tile's columns (D / 2) per CTA.
+  static constexpr int K_ROWS = PAIR ? BK / 2 : BK;
+  static constexpr int V_COLS = PAIR ? D / 2 : D;
   static constexpr int LA = (NQT == 1) ? 2 : 1;        // K tiles needed before the first P V
   static constexpr int SWB = (D * EB >= 128) ? 128 : D * EB;  // swizzle span in bytes
   static constexpr uint32_t SWZ = (SWB == 128) ? 2u : 4u;   // descriptor swizzle code
   static constexpr int RC = SWB / EB;                  // elements per swizzle region
   static constexpr int NR = D / RC;                    // regions per tile row
   static constexpr int Q_REGION = BQ * SWB;
-  static constexpr int KV_REGION = BK * SWB;
+  static constexpr int K_REGION = K_ROWS * SWB;        // one swizzle region of a K tile (slice)
+  static constexpr int V_REGION = BK * SWB;            // one swizzle region of a V tile (slice)
   static constexpr int Q_TILE = BQ * D * EB;
-  static constexpr int KV_TILE = BK * D * EB;
+  static constexpr int KV_TILE = K_ROWS * D * EB;      // shared-memory slot of one K or V tile (slice)
   static constexpr int P_COLS_64 = 64 * EB / 4;        // TMEM columns holding P of 64 keys
   static constexpr int NO = NQT;                       // O accumulators in TMEM
   // Two-tile mode at d = 128 issues each P V product as two runs over the key
@@ -136,25 +148,27 @@ struct TcCfg {
   static constexpr int MMA_WARP = SOFTMAX_WARPS + 4;
   static constexpr int LOAD_WARP = MMA_WARP + 1;
   static constexpr int THREADS = 32 * (SOFTMAX_WARPS + 8);  // + correction WG + MMA/TMA WG
-  // Register split (d <= 128).  Two tiles, 512 threads launched at 128
+  // Register split (d <= 128 and CTA pairs).  Two tiles, 512 threads launched at 128
   // registers each: softmax 176 and 160 between the correction and the
   // MMA/TMA warpgroups: 80 / 80, or 72 / 88 where that measured faster
   // (contiguous bf16 d = 64; the strided and e4m3 epilogues need the correction's 80);
   // 2*128*176 + 128*160 = 65536.  One tile, 384 threads launched at 168:
-  // softmax 208, correction 152, MMA/TMA 144; 128*(208 + 296) = 64512.
-  // d = 256 (one tile, 64-column S) fits 168 everywhere and is not split.
-  static constexpr bool SPLIT_REGS = (D <= 128);
+  // softmax 208, correction 152, MMA/TMA 144; 128*(208 + 296) = 64512
+  // (CTA pairs at d = 256: correction 160 for its 256-column rescale, 136).
+  // d = 256 on one CTA (64-column S) fits 168 everywhere and is not split.
+  static constexpr bool SPLIT_REGS = (D <= 128 || PAIR);
   static constexpr uint32_t REG_SOFTMAX = (NQT == 2) ? 176 : 208;
   static constexpr uint32_t REG_CORR_OTHER = (NQT == 2) ? 160 : 296;
   static constexpr __host__ __device__ uint32_t reg_corr(bool strided) {
-    return NQT == 1 ? 152 : ((!strided && D == 64 && !F8) ? 72 : 80);
+    return NQT == 1 ? (PAIR ? 160 : 152) : ((!strided && D == 64 && !FP8) ? 72 : 80);
   }
   static constexpr int LAUNCH_REGS = 65536 / THREADS > 255 ? 255 : (65536 / THREADS) & ~7;
   static_assert(!SPLIT_REGS || NQT * 128 * REG_SOFTMAX + 128 * REG_CORR_OTHER <= THREADS * LAUNCH_REGS,
                 "register split exceeds the launch budget");
   static_assert(D == 32 || D == 64 || D == 128 || D == 256, "head dim");
-  static_assert(!F8 || D == 64 || D == 128, "e4m3 kernels: d = 64 or 128");
+  static_assert(!FP8 || D == 64 || D == 128, "e4m3 kernels: d = 64 or 128");
   static_assert(SWB == 128 || SWB == 64, "swizzle span");
+  static_assert(!PAIR || (D == 256 && NQ == 1 && K_ROWS * D == BK * V_COLS), "CTA pairs: d = 256, one tile per CTA");
   static_assert(NQ == 1 || (NQ == 2 && D <= 128), "query tiles per unit");
   static_assert(NST >= 2, "K/V stages");
   static_assert(LA <= 2, "a stage holds at most two K tiles");
@@ -170,19 +184,19 @@ struct TcUnit {
   int nmax;
 };
 
-template <int D, bool CAUSAL, int NQ, bool F8>
+template <int D, bool CAUSAL, int NQ, int VAR>
 __device__ __forceinline__ TcUnit tc_decode(int u, const TcParams& p) {
-  using C = TcCfg<D, NQ, F8>;
+  using C = TcCfg<D, NQ, VAR>;
   TcUnit w;
   const int qb = p.n_qb - 1 - u / p.BH;  // heaviest query blocks first
   w.bh = u % p.BH;
-  w.row0 = qb * (C::BQ * C::NQT);
+  w.row0 = qb * (C::BQ * C::UNIT_TILES);
   w.nmax = 0;
 #pragma unroll
   for (int s = 0; s < 2; ++s) {
     const int r0 = w.row0 + s * C::BQ;
     int n = 0;
-    if (s < C::NQT && r0 < p.Nq) {
+    if (s < C::UNIT_TILES && r0 < p.Nq) {
       n = p.n_kv;
       if (CAUSAL) {
         const int last = (r0 + C::BQ - 1) / C::BK + 1;  // tiles holding keys <= last row
@@ -199,8 +213,11 @@ __device__ __forceinline__ TcUnit tc_decode(int u, const TcParams& p) {
 // them in rounds of gridDim.x, alternating direction every round (a snake),
 // so the CTA that takes the heaviest unit of one round takes the lightest of
 // the next and causal work evens out without any shared counter.
+template <bool PAIR = false>
 __device__ __forceinline__ int tc_unit(int k) {
-  const int g = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
+  // CTA pairs: the cluster (pair) is the unit of scheduling.
+  const int g = PAIR ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
+  const int b = PAIR ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
   return k * g + ((k & 1) ? g - 1 - b : b);
 }
 
@@ -208,7 +225,7 @@ __device__ __forceinline__ int tc_unit(int k) {
 // MMAs before the CTA exits); still time-limited.
 __device__ __forceinline__ bool wait_bar_drain(uint32_t bar, uint32_t parity, const WaitGuard& g) {
   const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!guard_try_wait(bar, parity, g)) {
     if (globaltimer_ns() - t0 > g.limit_ns) {
       atomicOr(g.status, kStatusTimeoutDrain);
       return false;
@@ -218,9 +235,9 @@ __device__ __forceinline__ bool wait_bar_drain(uint32_t bar, uint32_t parity, co
 }
 
 // Barrier addresses in shared memory.
-template <int D, int NQ, bool F8>
+template <int D, int NQ, int VAR>
 struct TcBars {
-  using C = TcCfg<D, NQ, F8>;
+  using C = TcCfg<D, NQ, VAR>;
   uint32_t b0;
   // Q tile t loaded / free again (one phase per work unit).
   __device__ __forceinline__ uint32_t q_full(int t) const { return b0 + 8u * t; }
@@ -258,12 +275,15 @@ struct TcBars {
 // the next unit.  Q tile t of the next unit is loaded after that last stage,
 // as soon as the current unit's last S_t product has completed (q_empty(t)).
 //
-// Single-tile mode: per unit, Q, then {K_0, K_1}, then {V_j, K_{j+2}}.
-template <int D, bool CAUSAL, bool STRIDED, int NQ, bool F8>
+// Single-tile mode: per unit, Q, then {K_0, K_1}, then {V_j, K_{j+2}}.  In a
+// CTA pair each CTA loads its own 128 Q rows, its half of the keys of every K
+// tile (BK / 2 rows) and its half of the columns of every V tile (D / 2),
+// all onto its own barriers.
+template <int D, bool CAUSAL, bool STRIDED, int NQ, int VAR>
 __device__ __forceinline__ void tc_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
-                                            const TcParams& p, const TcBars<D, NQ, F8>& bar, uint32_t base,
+                                            const TcParams& p, const TcBars<D, NQ, VAR>& bar, uint32_t base,
                                             const WaitGuard& g) {
-  using C = TcCfg<D, NQ, F8>;
+  using C = TcCfg<D, NQ, VAR>;
   const uint64_t pol_q = policy_evict_first();
   const uint64_t pol_kv = policy_evict_last();
   uint32_t pos = 0;       // stages issued so far
@@ -271,15 +291,25 @@ __device__ __forceinline__ void tc_producer(const CUtensorMap* tm_q, const CUten
   uint32_t last_par = 0;  // bit i: parity of stage i's latest load
   int last_q[2] = {-1, -1};  // per Q tile: index (within this CTA) of the latest unit whose tile was loaded
   bool ok = true;
-  // Tile j (rows j*BK ..) of unit bh.  Strided tensors are 4-D maps {d, N, H, B}
-  // (coordinates h, b), contiguous ones 3-D maps {d, N, B*H} (coordinate bh).
-  auto load_tile = [&](const CUtensorMap* tm, uint32_t dst, uint32_t full, int j, int bh) {
-    for (int r = 0; r < C::NR; ++r) {
+  const int rank = C::PAIR ? static_cast<int>(cluster_ctarank()) : 0;
+  // K tile j (rows j*BK ..; a pair CTA: its K_ROWS of them) and V tile j (a
+  // pair CTA: its V_COLS columns) of unit bh.  Strided tensors are 4-D maps
+  // {d, N, H, B} (coordinates h, b), contiguous ones 3-D maps {d, N, B*H}
+  // (coordinate bh).
+  auto load_slab = [&](const CUtensorMap* tm, uint32_t dst, uint32_t full, int x0, int row, int regions,
+                       int region_bytes, int bh) {
+    for (int r = 0; r < regions; ++r) {
       if constexpr (STRIDED)
-        tma_load_4d(dst + r * C::KV_REGION, tm, full, r * C::RC, j * C::BK, bh % p.H, bh / p.H, pol_kv);
+        tma_load_4d(dst + r * region_bytes, tm, full, x0 + r * C::RC, row, bh % p.H, bh / p.H, pol_kv);
       else
-        tma_load_3d(dst + r * C::KV_REGION, tm, full, r * C::RC, j * C::BK, bh, pol_kv);
+        tma_load_3d(dst + r * region_bytes, tm, full, x0 + r * C::RC, row, bh, pol_kv);
     }
+  };
+  auto load_k = [&](uint32_t dst, uint32_t full, int j, int bh) {
+    load_slab(tm_k, dst, full, 0, j * C::BK + rank * C::K_ROWS, C::NR, C::K_REGION, bh);
+  };
+  auto load_v = [&](uint32_t dst, uint32_t full, int j, int bh) {
+    load_slab(tm_v, dst, full, rank * C::V_COLS, j * C::BK, C::V_COLS / C::RC, C::V_REGION, bh);
   };
   // Q tiles of unit x, the qi-th unit of this CTA.
   auto load_q = [&](const TcUnit& x, int qi) -> bool {
@@ -292,7 +322,7 @@ __device__ __forceinline__ void tc_producer(const CUtensorMap* tm_q, const CUten
                       x.row0 + t * C::BQ, x.bh % p.H, x.bh / p.H, pol_q);
         else
           tma_load_3d(base + C::OFF_Q + t * C::Q_TILE + r * C::Q_REGION, tm_q, bar.q_full(t), r * C::RC,
-                      x.row0 + t * C::BQ, x.bh, pol_q);
+                      x.row0 + (t + rank) * C::BQ, x.bh, pol_q);
       last_q[t] = qi;
     }
     return true;
@@ -314,23 +344,23 @@ __device__ __forceinline__ void tc_producer(const CUtensorMap* tm_q, const CUten
 
   if constexpr (C::NQT == 2) {
     int uk = 0;
-    int u = tc_unit(0);
+    int u = tc_unit<C::PAIR>(0);
     if (u < p.total_units) {
-      TcUnit w = tc_decode<D, CAUSAL, NQ, F8>(u, p);
+      TcUnit w = tc_decode<D, CAUSAL, NQ, VAR>(u, p);
       uint32_t s0, full;
       ok = load_q(w, 0) && stage_begin(1, s0, full);
-      if (ok) load_tile(tm_k, s0, full, 0, w.bh);
+      if (ok) load_k(s0, full, 0, w.bh);
       while (ok) {
-        const int un = tc_unit(uk + 1);
+        const int un = tc_unit<C::PAIR>(uk + 1);
         const bool has_next = un < p.total_units;
-        const TcUnit wn = tc_decode<D, CAUSAL, NQ, F8>(has_next ? un : u, p);
+        const TcUnit wn = tc_decode<D, CAUSAL, NQ, VAR>(has_next ? un : u, p);
         for (int j = 0; ok && j < w.nmax; ++j) {
           const bool k_here = j + 1 < w.nmax;
           const bool k_next = !k_here && has_next;
           if (!(ok = stage_begin((k_here || k_next) ? 2 : 1, s0, full))) break;
-          load_tile(tm_v, s0, full, j, w.bh);
-          if (k_here) load_tile(tm_k, s0 + C::KV_TILE, full, j + 1, w.bh);
-          if (k_next) load_tile(tm_k, s0 + C::KV_TILE, full, 0, wn.bh);
+          load_v(s0, full, j, w.bh);
+          if (k_here) load_k(s0 + C::KV_TILE, full, j + 1, w.bh);
+          if (k_next) load_k(s0 + C::KV_TILE, full, 0, wn.bh);
         }
         if (!ok || !has_next) break;
         ++uk;
@@ -340,20 +370,20 @@ __device__ __forceinline__ void tc_producer(const CUtensorMap* tm_q, const CUten
       }
     }
   } else {
-    for (int uk = 0, u; ok && (u = tc_unit(uk)) < p.total_units; ++uk) {
-      const TcUnit w = tc_decode<D, CAUSAL, NQ, F8>(u, p);
+    for (int uk = 0, u; ok && (u = tc_unit<C::PAIR>(uk)) < p.total_units; ++uk) {
+      const TcUnit w = tc_decode<D, CAUSAL, NQ, VAR>(u, p);
       if (!(ok = load_q(w, uk))) break;
       uint32_t s0, full;
       for (int t = -1; t < w.nmax; ++t) {
         if (t < 0) {  // K_0 .. K_{LA-1}
           const int nk = C::LA < w.nmax ? C::LA : w.nmax;
           if (!(ok = stage_begin(nk, s0, full))) break;
-          for (int k = 0; k < nk; ++k) load_tile(tm_k, s0 + k * C::KV_TILE, full, k, w.bh);
+          for (int k = 0; k < nk; ++k) load_k(s0 + k * C::KV_TILE, full, k, w.bh);
         } else {  // V_t, K_{t+LA}
           const bool has_k = t + C::LA < w.nmax;
           if (!(ok = stage_begin(has_k ? 2 : 1, s0, full))) break;
-          load_tile(tm_v, s0, full, t, w.bh);
-          if (has_k) load_tile(tm_k, s0 + C::KV_TILE, full, t + C::LA, w.bh);
+          load_v(s0, full, t, w.bh);
+          if (has_k) load_k(s0 + C::KV_TILE, full, t + C::LA, w.bh);
         }
       }
     }
@@ -363,6 +393,13 @@ __device__ __forceinline__ void tc_producer(const CUtensorMap* tm_q, const CUten
     if (issued & (1u << i)) wait_bar_drain(bar.kv_full(i), (last_par >> i) & 1, g);
   for (int t = 0; t < C::NQT; ++t)
     if (last_q[t] >= 0) wait_bar_drain(bar.q_full(t), last_q[t] & 1, g);
+  // A pair CTA also waits for the leader's last releases of its stages and Q
+  // tile: those commits arrive on this CTA's barriers, which must still exist.
+  if constexpr (C::PAIR) {
+    for (int i = 0; i < C::NST; ++i)
+      if (issued & (1u << i)) wait_bar_drain(bar.kv_empty(i), (last_par >> i) & 1, g);
+    if (last_q[0] >= 0) wait_bar_drain(bar.q_empty(0), last_q[0] & 1, g);
+  }
 }
 
 // ------------------------------------------------------------------ MMA issuer
@@ -381,11 +418,13 @@ __device__ __forceinline__ void tc_producer(const CUtensorMap* tm_q, const CUten
 // Descriptors are kept as (low, high) words and built once: a tile position
 // or K step only adds a constant to the low word's address field (bits 0..13
 // hold address / 16, and no shared address reaches 2^18, so it never carries).
-template <int D, int NQ, bool F8>
+template <int D, int NQ, int VAR>
 struct TcMma {
-  using C = TcCfg<D, NQ, F8>;
-  static constexpr uint32_t IDESC_QK = F8 ? make_idesc_e4m3(128, C::BK, 0) : make_idesc_bf16(128, C::BK, 0);
-  static constexpr uint32_t IDESC_PV = F8 ? make_idesc_e4m3(128, D, 1) : make_idesc_bf16(128, D, 1);
+  using C = TcCfg<D, NQ, VAR>;
+  // M = 256 for a CTA pair (each CTA holds 128 of the rows).
+  static constexpr int MM = C::PAIR ? 256 : 128;
+  static constexpr uint32_t IDESC_QK = C::FP8 ? make_idesc_e4m3(MM, C::BK, 0) : make_idesc_bf16(MM, C::BK, 0);
+  static constexpr uint32_t IDESC_PV = C::FP8 ? make_idesc_e4m3(MM, D, 1) : make_idesc_bf16(MM, D, 1);
   static constexpr int N_QK = D * C::EB / 32;      // MMAs per S = Q K^T (K = d)
   static constexpr int N_PV = C::BK / C::KM;       // MMAs per P V (K = BK keys)
   // K-major (Q, K) and MN-major (V) operands share the stride byte offset
@@ -396,7 +435,7 @@ struct TcMma {
     return ((kk * C::KM / C::RC) * C::Q_REGION + (kk * C::KM % C::RC) * C::EB) >> 4;
   }
   static constexpr __host__ __device__ uint32_t k_step(int kk) {
-    return ((kk * C::KM / C::RC) * C::KV_REGION + (kk * C::KM % C::RC) * C::EB) >> 4;
+    return ((kk * C::KM / C::RC) * C::K_REGION + (kk * C::KM % C::RC) * C::EB) >> 4;
   }
   static constexpr __host__ __device__ uint32_t v_step(int kk) { return (kk * C::KM * C::SWB) >> 4; }
   static constexpr uint32_t TILE_STEP = C::KV_TILE >> 4;
@@ -410,7 +449,7 @@ struct TcMma {
   __device__ __forceinline__ TcMma(uint32_t tmem_, uint32_t base) : tmem(tmem_) {
     q_lo = sdesc_lo(base + C::OFF_Q, 16);
     k_lo = sdesc_lo(base + C::OFF_KV, 16);
-    v_lo = sdesc_lo(base + C::OFF_KV, C::KV_REGION);
+    v_lo = sdesc_lo(base + C::OFF_KV, C::V_REGION);
   }
   // Descriptor increments from K step k-1 to k.
   struct QkSteps {
@@ -429,11 +468,15 @@ struct TcMma {
     // d <= 128: one block per product (measured faster at d = 32 and 64, equal
     // at d = 128); d = 256: one MMA per block (measured faster there).
     if constexpr (D <= 128) {
-      mma_ss_run<N_QK, QkSteps, F8>(d_t, a, DESC_HI, b, DESC_HI, IDESC_QK, 0u);
+      mma_ss_run<N_QK, QkSteps, C::FP8>(d_t, a, DESC_HI, b, DESC_HI, IDESC_QK, 0u);
     } else {
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk)
-        mma_ss_elect(d_t, a + q_step(kk), DESC_HI, b + k_step(kk), DESC_HI, IDESC_QK, kk > 0 ? 1u : 0u);
+      for (int kk = 0; kk < D / 16; ++kk) {
+        if constexpr (C::PAIR)
+          mma_ss_pair(d_t, a + q_step(kk), DESC_HI, b + k_step(kk), DESC_HI, IDESC_QK, kk > 0 ? 1u : 0u);
+        else
+          mma_ss_elect(d_t, a + q_step(kk), DESC_HI, b + k_step(kk), DESC_HI, IDESC_QK, kk > 0 ? 1u : 0u);
+      }
     }
     commit(s_full_bar);
   }
@@ -443,11 +486,15 @@ struct TcMma {
     const uint32_t a_t = tmem + C::TM_S + buf * C::TM_SB;
     const uint32_t b = v_lo + vpos * TILE_STEP;
     if constexpr (D <= 128) {
-      mma_ts_run<N_PV, PvSteps, F8>(d_t, a_t, b, DESC_HI, IDESC_PV, acc ? 1u : 0u);
+      mma_ts_run<N_PV, PvSteps, C::FP8>(d_t, a_t, b, DESC_HI, IDESC_PV, acc ? 1u : 0u);
     } else {
 #pragma unroll
-      for (int kk = 0; kk < C::BK / 16; ++kk)
-        mma_ts_elect(d_t, a_t + kk * 8, b + v_step(kk), DESC_HI, IDESC_PV, (acc || kk > 0) ? 1u : 0u);
+      for (int kk = 0; kk < C::BK / 16; ++kk) {
+        if constexpr (C::PAIR)
+          mma_ts_pair(d_t, a_t + kk * 8, b + v_step(kk), DESC_HI, IDESC_PV, (acc || kk > 0) ? 1u : 0u);
+        else
+          mma_ts_elect(d_t, a_t + kk * 8, b + v_step(kk), DESC_HI, IDESC_PV, (acc || kk > 0) ? 1u : 0u);
+      }
     }
   }
   // O[ot] (+)= P[buf][:, 64h .. 64h+63] V[64h .. 64h+63, :]: one key half of
@@ -456,20 +503,27 @@ struct TcMma {
     const uint32_t d_t = tmem + C::TM_O + ot * D;
     const uint32_t a_t = tmem + C::TM_S + buf * C::TM_SB + h * C::P_COLS_64;
     const uint32_t b = v_lo + vpos * TILE_STEP + h * (64 * C::SWB / 16);
-    mma_ts_run<N_PV / 2, PvSteps, F8>(d_t, a_t, b, DESC_HI, IDESC_PV, acc ? 1u : 0u);
+    mma_ts_run<N_PV / 2, PvSteps, C::FP8>(d_t, a_t, b, DESC_HI, IDESC_PV, acc ? 1u : 0u);
   }
-  __device__ __forceinline__ void commit(uint32_t bar) const { mma_commit_elect(bar); }
+  // A CTA pair's commits arrive on the barrier at the same offset in both CTAs.
+  __device__ __forceinline__ void commit(uint32_t bar) const {
+    if constexpr (C::PAIR)
+      mma_commit_pair_mc(bar, 3);
+    else
+      mma_commit_elect(bar);
+  }
 };
 
-template <int D, bool CAUSAL, int NQ, bool F8>
-__device__ __forceinline__ void tc_mma(const TcParams& p, const TcBars<D, NQ, F8>& bar, uint32_t base, uint32_t tmem,
+template <int D, bool CAUSAL, int NQ, int VAR>
+__device__ __forceinline__ void tc_mma(const TcParams& p, const TcBars<D, NQ, VAR>& bar, uint32_t base, uint32_t tmem,
                                        const WaitGuard& g) {
-  using C = TcCfg<D, NQ, F8>;
-  const TcMma<D, NQ, F8> M(tmem, base);
+  using C = TcCfg<D, NQ, VAR>;
+  const TcMma<D, NQ, VAR> M(tmem, base);
   // Every lane waits (a non-blocking test first, then the bounded wait); the
   // outcome is made warp-uniform.
   auto wait = [&](uint32_t b, uint32_t par) -> bool {
-    const bool r = mbar_test_wait(b, par) || wait_bar(b, par, g, kStatusTimeoutMma);
+    const bool r = (C::PAIR ? mbar_test_wait_cl(b, par) : mbar_test_wait(b, par)) ||
+                   wait_bar(b, par, g, kStatusTimeoutMma);
     return __all_sync(0xffffffffu, r);
   };
   uint32_t pos = 0;               // K/V stages consumed
@@ -500,7 +554,7 @@ __device__ __forceinline__ void tc_mma(const TcParams& p, const TcBars<D, NQ, F8
     // S_t product.  The next unit's first products still wait for O_t to be
     // read out by the epilogue (there is no room in TMEM for a second O).
     int uk = 0;
-    int u = tc_unit(0);
+    int u = tc_unit<C::PAIR>(0);
     // S_t for key tile 0 of unit x (the qi-th unit), K_0 at position kpos.
     auto first_qk = [&](const TcUnit& x, int qi, int t, uint32_t kpos) -> bool {
       if (!wait(bar.q_full(t), qi & 1)) return false;
@@ -540,14 +594,14 @@ __device__ __forceinline__ void tc_mma(const TcParams& p, const TcBars<D, NQ, F8
       return true;
     };
     if (u < p.total_units) {
-      TcUnit w = tc_decode<D, CAUSAL, NQ, F8>(u, p);
+      TcUnit w = tc_decode<D, CAUSAL, NQ, VAR>(u, p);
       uint32_t st;
       ok = stage_acquire(st) && first_qk(w, 0, 0, 2 * st) && first_qk(w, 0, 1, 2 * st);
       if (ok) M.commit(bar.kv_empty(st));
       while (ok) {
-        const int un = tc_unit(uk + 1);
+        const int un = tc_unit<C::PAIR>(uk + 1);
         const bool has_next = un < p.total_units;
-        const TcUnit wn = tc_decode<D, CAUSAL, NQ, F8>(has_next ? un : u, p);
+        const TcUnit wn = tc_decode<D, CAUSAL, NQ, VAR>(has_next ? un : u, p);
         for (int j = 0; ok && j < w.nmax; ++j) {
           if (!(ok = stage_acquire(st))) break;
           // In a unit's last step both P V products go first: the next unit's
@@ -568,12 +622,12 @@ __device__ __forceinline__ void tc_mma(const TcParams& p, const TcBars<D, NQ, F8
     }
   } else {
     uint32_t qk_total = 0;  // S products issued so far
-    for (int uk = 0, u; ok && (u = tc_unit(uk)) < p.total_units; ++uk) {
-      const TcUnit w = tc_decode<D, CAUSAL, NQ, F8>(u, p);
+    for (int uk = 0, u; ok && (u = tc_unit<C::PAIR>(uk)) < p.total_units; ++uk) {
+      const TcUnit w = tc_decode<D, CAUSAL, NQ, VAR>(u, p);
       if (!(ok = wait(bar.q_full(0), uk & 1))) break;
       uint32_t st;
       if (!(ok = stage_acquire(st))) break;
-      const int n = w.n[0];
+      const int n = C::PAIR ? w.nmax : w.n[0];  // a pair visits every key tile either CTA's rows need
       const uint32_t qk_base = qk_total;  // S product of key tile j sits in buffer (qk_base + j) & 1
       // First stage: K_0, K_1.
       for (int t = 0; t < C::LA && t < n; ++t) {
@@ -598,9 +652,41 @@ __device__ __forceinline__ void tc_mma(const TcParams& p, const TcBars<D, NQ, F8
     }
   }
   (void)go1;
-  // All issued MMAs must complete before TMEM is released.
-  M.commit(bar.drain());
+  // All issued MMAs must complete before TMEM is released (a pair: this CTA's
+  // barrier only).
+  if constexpr (C::PAIR)
+    mma_commit_pair_mc(bar.drain(), 1);
+  else
+    M.commit(bar.drain());
   wait_bar_drain(bar.drain(), 0, g);
+  __syncwarp();
+}
+
+// ------------------------------------------------------------------ pair forwarder
+// Run by the MMA warp of a CTA pair's second CTA (rank 1), which issues no
+// MMAs: in the producer's order, wait for each phase of this CTA's Q and K/V
+// barriers (its own copies have landed) and arrive on the leader's barrier at
+// the same offset, so that the leader's MMA warp sees both halves loaded.
+template <int D, bool CAUSAL, int NQ, int VAR>
+__device__ __forceinline__ void tc_forward(const TcParams& p, const TcBars<D, NQ, VAR>& bar, const WaitGuard& g) {
+  using C = TcCfg<D, NQ, VAR>;
+  const int lane = threadIdx.x & 31;
+  uint32_t pos = 0;  // stages forwarded
+  auto forward = [&](uint32_t b, uint32_t par) -> bool {
+    if (!warp_wait_bar(b, par, g, kStatusTimeoutLoad)) return false;
+    __syncwarp();
+    if (lane == 0) mbar_arrive_cluster(mapa_shared(b, 0));
+    return true;
+  };
+  bool ok = true;
+  for (int uk = 0, u; ok && (u = tc_unit<C::PAIR>(uk)) < p.total_units; ++uk) {
+    const TcUnit w = tc_decode<D, CAUSAL, NQ, VAR>(u, p);
+    ok = forward(bar.q_full(0), uk & 1);
+    for (int t = -1; ok && t < w.nmax; ++t) {  // the first stage (K_0, K_1), then one per key tile
+      ok = forward(bar.kv_full(pos % C::NST), (pos / C::NST) & 1);
+      ++pos;
+    }
+  }
   __syncwarp();
 }
 
@@ -613,11 +699,24 @@ __device__ __forceinline__ float ld_shared_volatile(const float* p) {
   return v;
 }
 
-template <int D, bool CAUSAL, int NQ, bool F8>
-__device__ __forceinline__ void tc_softmax(const TcParams& p, const TcBars<D, NQ, F8>& bar, uint8_t* gbase, uint32_t tmem,
+// Warp arrival on barrier `bar` of the CTA that issues the MMAs: this CTA's
+// own, or for a CTA pair the leader's barrier at the same offset.
+template <bool PAIR>
+__device__ __forceinline__ void arrive_issuer(uint32_t bar) {
+  if constexpr (PAIR) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive_cluster(mapa_shared(bar, 0));
+  } else {
+    warp_arrive(bar);
+  }
+}
+
+template <int D, bool CAUSAL, int NQ, int VAR>
+__device__ __forceinline__ void tc_softmax(const TcParams& p, const TcBars<D, NQ, VAR>& bar, uint8_t* gbase, uint32_t tmem,
                                            int wg, int quarter, int lane, const WaitGuard& g) {
-  using C = TcCfg<D, NQ, F8>;
+  using C = TcCfg<D, NQ, VAR>;
   const int r = quarter * 32 + lane;  // row within the query tile = TMEM lane
+  const int rank = C::PAIR ? static_cast<int>(cluster_ctarank()) : 0;  // a pair CTA's tile within the unit
   const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
   const int ot = (C::NQT == 2) ? wg : 0;
   // alpha of rescale step number k (counted over this accumulator) goes to slot k & 1: in
@@ -632,11 +731,13 @@ __device__ __forceinline__ void tc_softmax(const TcParams& p, const TcBars<D, NQ
   uint32_t s_waits = 0;  // S buffers consumed by this warpgroup
   bool ok = true;
 
-  for (int uk = 0, u; ok && (u = tc_unit(uk)) < p.total_units; ++uk) {
-    const TcUnit w = tc_decode<D, CAUSAL, NQ, F8>(u, p);
-    const int n = w.n[wg];
+  for (int uk = 0, u; ok && (u = tc_unit<C::PAIR>(uk)) < p.total_units; ++uk) {
+    const TcUnit w = tc_decode<D, CAUSAL, NQ, VAR>(u, p);
+    // A pair CTA takes part in every key tile of the unit (its rows may see
+    // none of a tile's keys: then P = 0 and alpha = 1 for them).
+    const int n = C::PAIR ? w.nmax : w.n[wg];
     if (n == 0) continue;
-    const int row0 = w.row0 + wg * C::BQ;
+    const int row0 = w.row0 + (wg + rank) * C::BQ;
     const int row = row0 + r;
     float m = -INFINITY;  // running max of scaled logits, log2 units
     float l = 0.f;        // running sum of exp2(x - m)
@@ -752,7 +853,7 @@ __device__ __forceinline__ void tc_softmax(const TcParams& p, const TcBars<D, NQ
       tmem_wait_st();
       tc_fence_before();
       // P number s_waits - 1 (counted over this warpgroup) feeds P V number s_waits - 1.
-      warp_arrive(C::NQT == 2 ? bar.pv_go(ot, C::PV_SPLIT ? 1 : 0) : bar.pv_go(0, (s_waits - 1) & 1));
+      arrive_issuer<C::PAIR>(C::NQT == 2 ? bar.pv_go(ot, C::PV_SPLIT ? 1 : 0) : bar.pv_go(0, (s_waits - 1) & 1));
     }
     if (!ok) break;
     stat_m[(uk & 1) * 256 + r] = m;
@@ -762,12 +863,13 @@ __device__ __forceinline__ void tc_softmax(const TcParams& p, const TcBars<D, NQ
 }
 
 // ------------------------------------------------------------------ correction + epilogue
-template <int D, bool CAUSAL, bool STRIDED, int NQ, bool F8>
-__device__ __forceinline__ void tc_correction(const TcParams& p, const CUtensorMap* tm_o, const TcBars<D, NQ, F8>& bar,
+template <int D, bool CAUSAL, bool STRIDED, int NQ, int VAR>
+__device__ __forceinline__ void tc_correction(const TcParams& p, const CUtensorMap* tm_o, const TcBars<D, NQ, VAR>& bar,
                                               uint8_t* gbase, uint32_t tmem, int quarter, int lane,
                                               const WaitGuard& g) {
-  using C = TcCfg<D, NQ, F8>;
+  using C = TcCfg<D, NQ, VAR>;
   const int r = quarter * 32 + lane;
+  const int rank = C::PAIR ? static_cast<int>(cluster_ctarank()) : 0;  // a pair CTA's tile within the unit
   const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
   const float* alpha_base = reinterpret_cast<const float*>(gbase + C::OFF_ALPHA);
   const float* stat_m = reinterpret_cast<const float*>(gbase + C::OFF_STAT_M);
@@ -783,7 +885,7 @@ __device__ __forceinline__ void tc_correction(const TcParams& p, const CUtensorM
     if (C::NQT == 2) {
       warp_arrive(bar.pv_go(t, 0));
     } else {
-      warp_arrive(bar.pv_go(0, go_arr & 1));
+      arrive_issuer<C::PAIR>(bar.pv_go(0, go_arr & 1));
       ++go_arr;
     }
   };
@@ -853,8 +955,8 @@ __device__ __forceinline__ void tc_correction(const TcParams& p, const CUtensorM
     const float lrow = stat_l[su * 256 + t * 128 + r];
     const float inv_l = (C::FP8 ? p.o_scale : 1.f) / lrow;
     const uint64_t il2 = f2_pack(inv_l, inv_l);
-    const int row = w.row0 + t * C::BQ + r;
-    const int wrow0 = w.row0 + t * C::BQ + quarter * 32;  // first row of this warp's box
+    const int row = w.row0 + (t + rank) * C::BQ + r;
+    const int wrow0 = w.row0 + (t + rank) * C::BQ + quarter * 32;  // first row of this warp's box
     const uint32_t to = tmem + lane_off + C::TM_O + t * D;
     const uint32_t sw = static_cast<uint32_t>((lane >> 1) & 3);
 #pragma unroll 1
@@ -900,13 +1002,14 @@ __device__ __forceinline__ void tc_correction(const TcParams& p, const CUtensorM
   // O starts free: release it for the first unit's first P V.
   release_o(0);
   if (C::NO == 2) release_o(1);
-  for (int uk = 0, u; ok && (u = tc_unit(uk)) < p.total_units; ++uk) {
-    const TcUnit w = tc_decode<D, CAUSAL, NQ, F8>(u, p);
+  for (int uk = 0, u; ok && (u = tc_unit<C::PAIR>(uk)) < p.total_units; ++uk) {
+    const TcUnit w = tc_decode<D, CAUSAL, NQ, VAR>(u, p);
     // Same order as the MMA warp's P V products: (tile 0, j), (tile 1, j), (tile 0, j+1), ...
+    const int n0 = C::PAIR ? w.nmax : w.n[0];  // a pair CTA takes part in every key tile of the unit
     for (int j = 0; ok && j < w.nmax; ++j) {
-      if (ok && j >= 1 && j < w.n[0]) ok = rescale(0, a_cnt0, od0);
+      if (ok && j >= 1 && j < n0) ok = rescale(0, a_cnt0, od0);
       if (C::NO == 2 && ok && j >= 1 && j < w.n[1]) ok = rescale(1, a_cnt1, od1);
-      if (ok && j == w.n[0] - 1) ok = epilogue(w, uk & 1, 0, od0, lf0);
+      if (ok && j == n0 - 1) ok = epilogue(w, uk & 1, 0, od0, lf0);
       if (C::NO == 2 && ok && j == w.n[1] - 1) ok = epilogue(w, uk & 1, 1, od1, lf1);
     }
   }
@@ -916,36 +1019,42 @@ __device__ __forceinline__ void tc_correction(const TcParams& p, const CUtensorM
 }
 
 // ------------------------------------------------------------------ kernel
-template <int D, bool CAUSAL, bool STRIDED, int NQ, bool F8>
-__global__ void __launch_bounds__(TcCfg<D, NQ, F8>::THREADS, 1)
+template <int D, bool CAUSAL, bool STRIDED, int NQ, int VAR>
+__global__ void __launch_bounds__(TcCfg<D, NQ, VAR>::THREADS, 1)
     fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                      const TcParams p) {
-  using C = TcCfg<D, NQ, F8>;
+  using C = TcCfg<D, NQ, VAR>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const TcBars<D, NQ, F8> bar{base + C::OFF_BAR};
+  const TcBars<D, NQ, VAR> bar{base + C::OFF_BAR};
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::OFF_TMEM_SLOT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::OFF_ABORT);
+  // CTA pairs: rank 0 (the leader) issues the MMAs; its Q and K/V barriers
+  // also take the arrival forwarded by rank 1, and its P V barriers the
+  // arrivals of both CTAs' softmax and correction warps.
+  const uint32_t rank = C::PAIR ? cluster_ctarank() : 0;
+  const uint32_t full_count = (C::PAIR && rank == 0) ? 2 : 1;
+  const uint32_t go_count = C::PAIR ? 16 : 8;
 
   if (threadIdx.x == 0) {
     for (int t = 0; t < 2; ++t) {
-      mbar_init(bar.q_full(t), 1);
+      mbar_init(bar.q_full(t), full_count);
       mbar_init(bar.q_empty(t), 1);
     }
     for (int i = 0; i < C::NST; ++i) {
-      mbar_init(bar.kv_full(i), 1);
+      mbar_init(bar.kv_full(i), full_count);
       mbar_init(bar.kv_empty(i), 1);
     }
     for (int b = 0; b < 2; ++b) {
       // Signalled by warps (one arrival each) or by tcgen05.commit (one).
       mbar_init(bar.s_full(b), 1);
-      mbar_init(bar.pv_go(b, 0), 8);  // 4 softmax warps + 4 correction warps
-      mbar_init(bar.pv_go(b, 1), C::PV_SPLIT ? 4 : 8);  // split P V: second key half, 4 softmax warps
+      mbar_init(bar.pv_go(b, 0), go_count);  // 4 softmax warps + 4 correction warps (per CTA of a pair)
+      mbar_init(bar.pv_go(b, 1), C::PV_SPLIT ? 4 : go_count);  // split P V: second key half, 4 softmax warps
       mbar_init(bar.a_full(b, 0), 4);
       mbar_init(bar.a_full(b, 1), 4);
       mbar_init(bar.o_done(b), 1);
@@ -962,33 +1071,52 @@ __global__ void __launch_bounds__(TcCfg<D, NQ, F8>::THREADS, 1)
     prefetch_tmap(&tm_o);
   }
   if (warp == C::MMA_WARP) {
-    tmem_alloc(smem_u32(tmem_slot), C::TM_COLS);
-    tmem_relinquish();
+    if constexpr (C::PAIR) {
+      tmem_alloc_pair(smem_u32(tmem_slot), C::TM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), C::TM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  // Both CTAs of a pair have initialised their barriers before either
+  // arrives on, or commits to, the other's.
+  if constexpr (C::PAIR) cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const WaitGuard g{abort_flag, p.status, p.limit_ns};
+  const WaitGuard g{abort_flag, p.status, p.limit_ns, C::PAIR};
 
   if (warp < C::SOFTMAX_WARPS) {
     if constexpr (C::SPLIT_REGS) regs_increase<C::REG_SOFTMAX>();
-    tc_softmax<D, CAUSAL, NQ, F8>(p, bar, gbase, tmem, warp >> 2, warp & 3, lane, g);
+    tc_softmax<D, CAUSAL, NQ, VAR>(p, bar, gbase, tmem, warp >> 2, warp & 3, lane, g);
   } else if (warp < C::SOFTMAX_WARPS + 4) {
     if constexpr (C::SPLIT_REGS) regs_decrease<C::reg_corr(STRIDED)>();
-    tc_correction<D, CAUSAL, STRIDED, NQ, F8>(p, &tm_o, bar, gbase, tmem, warp & 3, lane, g);
+    tc_correction<D, CAUSAL, STRIDED, NQ, VAR>(p, &tm_o, bar, gbase, tmem, warp & 3, lane, g);
   } else {
     if constexpr (C::SPLIT_REGS) regs_decrease<C::REG_CORR_OTHER - C::reg_corr(STRIDED)>();
-    if (warp == C::LOAD_WARP && lane == 0) tc_producer<D, CAUSAL, STRIDED, NQ, F8>(&tm_q, &tm_k, &tm_v, p, bar, base, g);
-    if (warp == C::MMA_WARP) tc_mma<D, CAUSAL, NQ, F8>(p, bar, base, tmem, g);
+    if (warp == C::LOAD_WARP && lane == 0) tc_producer<D, CAUSAL, STRIDED, NQ, VAR>(&tm_q, &tm_k, &tm_v, p, bar, base, g);
+    if (warp == C::MMA_WARP) {
+      if (rank == 0)
+        tc_mma<D, CAUSAL, NQ, VAR>(p, bar, base, tmem, g);
+      else
+        tc_forward<D, CAUSAL, NQ, VAR>(p, bar, g);
+    }
   }
 
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  // A pair CTA leaves only once the other is done with its shared memory,
+  // barriers and TMEM (the leader's MMAs read and write both CTAs').
+  if constexpr (C::PAIR) cluster_sync_all();
   if (warp == C::MMA_WARP) {
     tc_fence_after();
-    tmem_dealloc(tmem, C::TM_COLS);
+    if constexpr (C::PAIR)
+      tmem_dealloc_pair(tmem, C::TM_COLS);
+    else
+      tmem_dealloc(tmem, C::TM_COLS);
   }
 }
 

@@ -63,6 +63,62 @@ __device__ __forceinline__ uint32_t mbar_test_wait(uint32_t bar, uint32_t parity
   return ok;
 }
 
+// Cluster-scope forms (CTA pairs): wait with acquire at cluster scope, so that
+// what the other CTA of the cluster released before arriving is visible.
+__device__ __forceinline__ uint32_t mbar_try_wait_cl(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred P1;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 P1, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, P1;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok;
+}
+__device__ __forceinline__ uint32_t mbar_test_wait_cl(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred P1;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 P1, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, P1;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok;
+}
+
+// Address in the shared::cluster window of the same shared-memory offset in
+// the cluster's CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// Arrive (release at cluster scope) on a barrier given by its shared::cluster address.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_count_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster arrives (release) and waits (acquire).
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Error bits written to the device status word.
 enum : int {
   kStatusTimeoutLoad = 1 << 0,
@@ -76,17 +132,22 @@ struct WaitGuard {
   volatile int* abort;  // shared memory flag, set once any wait of the CTA gives up
   int* status;          // device status word (global memory)
   uint64_t limit_ns;
+  bool cluster = false;  // CTA pairs: waits acquire at cluster scope
 };
+
+__device__ __forceinline__ uint32_t guard_try_wait(uint32_t bar, uint32_t parity, const WaitGuard& g) {
+  return g.cluster ? mbar_try_wait_cl(bar, parity) : mbar_try_wait(bar, parity);
+}
 
 // Wait for the phase of `bar` with parity `parity` to complete.  Returns
 // false (without completing) if the CTA's abort flag is raised or the wait
 // exceeds the time limit; in the latter case this thread raises the flag and
 // ORs `code` into the status word.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const WaitGuard& g, int code) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (guard_try_wait(bar, parity, g)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (guard_try_wait(bar, parity, g)) return true;
     if (*g.abort) return false;
     if (globaltimer_ns() - t0 > g.limit_ns) {
       *g.abort = 1;
@@ -219,6 +280,18 @@ __device__ __forceinline__ void tmem_relinquish() {
 
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// CTA pairs: one warp in each CTA of the pair executes these together.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -600,6 +673,43 @@ __device__ __forceinline__ void mma_ts_run(uint32_t d_tmem, uint32_t a_tmem, uin
     if constexpr (N == 6) mma_ts_x6<S>(d_tmem, a_tmem, b_lo, b_hi, idesc, accumulate);
     if constexpr (N == 8) mma_ts_x8<S>(d_tmem, a_tmem, b_lo, b_hi, idesc, accumulate);
   }
+}
+
+// CTA-pair MMAs (cta_group::2, M = 256): A rows 0..127 from this CTA, 128..255
+// from the peer at the same address; B's N columns half from each CTA; D rows
+// split the same way across the two CTAs' TMEM.  Issued by the pair's leader.
+__device__ __forceinline__ void mma_ss_pair(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
+                                            uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred P1, PE;\n\t.reg .b64 DA, DB;\n\t"
+      "setp.ne.b32 P1, %6, 0;\n\t"
+      "mov.b64 DA, {%1, %2};\n\t"
+      "mov.b64 DB, {%3, %4};\n\t"
+      "elect.sync _|PE, 0xffffffff;\n\t"
+      "@PE tcgen05.mma.cta_group::2.kind::f16 [%0], DA, DB, %5, P1;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred P1, PE;\n\t.reg .b64 DB;\n\t"
+      "setp.ne.b32 P1, %5, 0;\n\t"
+      "mov.b64 DB, {%2, %3};\n\t"
+      "elect.sync _|PE, 0xffffffff;\n\t"
+      "@PE tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], DB, %4, P1;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive once on the barrier at offset `bar` of every CTA in `mask` when the
+// pair MMAs this warp issued so far have completed.
+__device__ __forceinline__ void mma_commit_pair_mc(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "{\n\t.reg .pred PE;\n\t"
+      "elect.sync _|PE, 0xffffffff;\n\t"
+      "@PE tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}"
+      ::"r"(bar), "h"(mask)
+      : "memory");
 }
 
 // Arrive once on `bar` when every tcgen05 operation the warp issued so far
