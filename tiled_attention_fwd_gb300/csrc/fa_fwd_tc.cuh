@@ -188,8 +188,18 @@ template <int D, bool CAUSAL, int NQ, int VAR>
 __device__ __forceinline__ TcUnit tc_decode(int u, const TcParams& p) {
   using C = TcCfg<D, NQ, VAR>;
   TcUnit w;
-  const int qb = p.n_qb - 1 - u / p.BH;  // heaviest query blocks first
-  w.bh = u % p.BH;
+  // Causal: heaviest query blocks first (all heads' block n_qb - 1, then
+  // n_qb - 2, ...), which balances the persistent CTAs.  Without the mask
+  // every unit costs the same, so units run head by head instead: the CTAs
+  // working at one time then share a few heads' K and V in L2.
+  int qb;
+  if (CAUSAL) {
+    qb = p.n_qb - 1 - u / p.BH;
+    w.bh = u % p.BH;
+  } else {
+    qb = u % p.n_qb;
+    w.bh = u / p.n_qb;
+  }
   w.row0 = qb * (C::BQ * C::UNIT_TILES);
   w.nmax = 0;
 #pragma unroll
