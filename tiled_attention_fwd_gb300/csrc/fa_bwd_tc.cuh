@@ -127,15 +127,25 @@ struct BwdUnit {
 // Units are numbered heaviest first under the causal mask: in MODE 0 the
 // first key tiles see the most query tiles, in MODE 1 the last query tiles
 // see the most key tiles.  Streamed tiles that lie wholly on the masked side
-// of the diagonal are skipped.
+// of the diagonal are skipped.  Without the mask every unit costs the same
+// and units are numbered head by head, so that the CTAs at work at one time
+// share a few heads' streamed tiles in L2.
 template <int D, int MODE, bool CAUSAL>
 __device__ __forceinline__ BwdUnit bwd_decode(int u, const BwdParams& p) {
   constexpr int HV = BwdCfg<D, MODE>::HALVES;
   BwdUnit w;
-  const int per_tile = p.BH * HV;  // units per fixed tile
-  const int mt = (MODE == 0) ? (u / per_tile) : (p.n_m - 1 - u / per_tile);
-  w.half = (u % per_tile) / p.BH;
-  w.bh = u % p.BH;
+  int mt;
+  if (CAUSAL) {
+    const int per_tile = p.BH * HV;  // units per fixed tile
+    mt = (MODE == 0) ? (u / per_tile) : (p.n_m - 1 - u / per_tile);
+    w.half = (u % per_tile) / p.BH;
+    w.bh = u % p.BH;
+  } else {
+    const int per_head = p.n_m * HV;  // units per head
+    w.bh = u / per_head;
+    mt = (u % per_head) / HV;
+    w.half = u % HV;
+  }
   w.m0 = mt * 128;
   if (MODE == 0) {
     w.s_begin = CAUSAL ? w.m0 / BwdCfg<D, MODE>::BS : 0;  // query tiles holding some query >= the first key
