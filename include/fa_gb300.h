@@ -183,8 +183,12 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
  * exp(scale * Q K^T - L) ("FlashAttention-2 from PyTorch to Triton", "What We
  * Are Building"); as in the metal-flash-attention backward ("Case Study:
  * metal-flash-attention") a dK/dV kernel and a dQ kernel each own their
- * outputs, so the results are deterministic (no atomics).  Three kernels are
- * enqueued on `stream`: D = rowsum(dO * O), dK/dV, dQ.
+ * outputs, so the results are deterministic (no atomics).  Three kernels:
+ * D = rowsum(dO * O) and the dK/dV kernel on `stream`, and the dQ kernel on a
+ * second stream of the library that starts after the first kernel and that
+ * `stream` waits for at the end, so the dQ kernel takes the SMs the dK/dV
+ * kernel frees as it finishes; the call is ordered on `stream` like a single
+ * kernel (also under stream capture).
  *
  *   q, k, v, o, dout : device pointers to bf16 [B][H][N][d], 16-byte aligned;
  *                      o and lse are the outputs of fa_fwd for q, k, v, scale, causal.

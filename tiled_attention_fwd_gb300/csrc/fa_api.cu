@@ -30,6 +30,16 @@ struct HostPipeline {
   cudaEvent_t done[kHostChunks] = {};
 };
 
+// The backward pass's second stream: the dQ kernel runs on it beside the
+// dK/dV kernel (both forked from and joined to the caller's stream).
+struct BwdFork {
+  bool ready = false;
+  std::mutex mutex;  // one enqueue sequence at a time (the events are reused)
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr;
+  cudaEvent_t join = nullptr;
+};
+
 struct DeviceState {
   bool ready = false;
   int* status = nullptr;  // one device int, zeroed at creation
@@ -37,6 +47,7 @@ struct DeviceState {
   int cc_major = 0;
   int cc_minor = 0;
   HostPipeline pipe;
+  BwdFork bwd;
 };
 
 std::mutex g_mutex;
@@ -423,6 +434,21 @@ namespace {
 
 // Checks shared by fa_bwd and fa_bwd_strided, then the launch.  The strides in
 // a.st are already validated by the caller; `strided` selects the 4-D maps.
+// Create the backward pass's second stream and events for device state `s` (once).
+int bwd_fork(DeviceState* s, BwdFork** out) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  BwdFork& f = s->bwd;
+  if (!f.ready) {
+    if (cudaStreamCreateWithFlags(&f.side, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&f.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&f.join, cudaEventDisableTiming) != cudaSuccess)
+      return FA_ERR_CUDA;
+    f.ready = true;
+  }
+  *out = &f;
+  return FA_OK;
+}
+
 int run_bwd(BwdArgs& a, int d, bool strided, void* workspace, size_t workspace_bytes, void* stream) {
   if (!a.q || !a.k || !a.v || !a.o || !a.lse || !a.dout || !a.dq || !a.dk || !a.dv || !workspace)
     return FA_ERR_NULL_POINTER;
@@ -434,7 +460,14 @@ int run_bwd(BwdArgs& a, int d, bool strided, void* workspace, size_t workspace_b
   DeviceState* s = nullptr;
   int rc = current_device_state(&s);
   if (rc != FA_OK) return rc;
-  const LaunchCtx ctx = make_ctx(*s, stream);
+  LaunchCtx ctx = make_ctx(*s, stream);
+  BwdFork* f = nullptr;
+  rc = bwd_fork(s, &f);
+  if (rc != FA_OK) return rc;
+  std::lock_guard<std::mutex> lock(f->mutex);
+  ctx.side = f->side;
+  ctx.ev_fork = f->fork;
+  ctx.ev_join = f->join;
   a.n_pad = (a.Nq + 191) / 192 * 192;
   a.l2 = static_cast<float*>(workspace);
   a.dsum = reinterpret_cast<float*>(static_cast<char*>(workspace) +

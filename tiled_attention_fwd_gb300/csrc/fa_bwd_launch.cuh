@@ -73,9 +73,27 @@ int launch_bwd_impl(const BwdArgs& a, const LaunchCtx& ctx) {
                                                       a.B * a.H, a.H, a.Nq, a.n_pad, ps);
   int e = static_cast<int>(cudaGetLastError());
   if (e != 0) return e;
+  // The dK/dV and dQ kernels are independent once the preprocessing is done:
+  // the dQ kernel runs on a second stream forked after the preprocessing, so
+  // that its CTAs take the SMs the dK/dV kernel frees at its tail; the
+  // caller's stream then waits for it (ordered on `stream` like one kernel).
+  LaunchCtx q_ctx = ctx;
+  if (ctx.side != nullptr) {
+    if (cudaEventRecord(ctx.ev_fork, ctx.stream) != cudaSuccess ||
+        cudaStreamWaitEvent(ctx.side, ctx.ev_fork, 0) != cudaSuccess)
+      return -1;
+    q_ctx.stream = ctx.side;
+  }
   e = a.causal ? launch_bwd_main<D, 0, true, STRIDED>(a, ctx) : launch_bwd_main<D, 0, false, STRIDED>(a, ctx);
   if (e != 0) return e;
-  return a.causal ? launch_bwd_main<D, 1, true, STRIDED>(a, ctx) : launch_bwd_main<D, 1, false, STRIDED>(a, ctx);
+  e = a.causal ? launch_bwd_main<D, 1, true, STRIDED>(a, q_ctx) : launch_bwd_main<D, 1, false, STRIDED>(a, q_ctx);
+  if (e != 0) return e;
+  if (ctx.side != nullptr) {
+    if (cudaEventRecord(ctx.ev_join, ctx.side) != cudaSuccess ||
+        cudaStreamWaitEvent(ctx.stream, ctx.ev_join, 0) != cudaSuccess)
+      return -1;
+  }
+  return 0;
 }
 
 }  // namespace fa

@@ -16,6 +16,11 @@ struct LaunchCtx {
   unsigned long long limit_ns;    // time limit of each device-side wait
   int num_sms;                    // SMs of the current device
   cudaStream_t stream;
+  // Backward pass: a second stream for the dQ kernel and the events that fork
+  // it from and join it to `stream` (null: everything on `stream`).
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_fork = nullptr;
+  cudaEvent_t ev_join = nullptr;
 };
 
 // Arguments of the bf16 forward pass.  Each of q, k, v, o is addressed as
