@@ -105,8 +105,11 @@ struct TcCfg {
   // halves of P (64 keys each), the first as soon as the softmax has written
   // the first half of P, so the tensor core starts while the second half's
   // exponentials are computed (+1.6 % at d = 128 non-causal and at N = 16384
-  // causal; at d <= 64 the extra store wait in the softmax cost 2-3 %).
-  static constexpr bool PV_SPLIT = (NQT == 2 && D == 128);
+  // causal; at d <= 64 the extra store wait in the softmax cost 2-3 %).  The
+  // e4m3 kernel issues each P V product whole: there its two runs of K = 64
+  // keys are half as many MMAs as in bf16, and the split measured 1.1-1.3 %
+  // slower on all three d = 128 e4m3 workloads.
+  static constexpr bool PV_SPLIT = (NQT == 2 && D == 128 && !FP8);
   // Shared memory: [Q tiles][K/V stages][misc]; misc = barriers, alpha, m/l, TMEM address, abort flag.
   static constexpr int MISC = 7168;
   static constexpr int SMEM_LIMIT = 227 * 1024;
