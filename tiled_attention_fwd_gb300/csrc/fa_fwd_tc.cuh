@@ -704,14 +704,6 @@ __device__ __forceinline__ void tc_forward(const TcParams& p, const TcBars<D, NQ
 }
 
 // ------------------------------------------------------------------ softmax
-// Shared-memory load that the compiler keeps in program order with the
-// surrounding barrier operations.
-__device__ __forceinline__ float ld_shared_volatile(const float* p) {
-  float v;
-  asm volatile("ld.volatile.shared.f32 %0, [%1];" : "=f"(v) : "r"(smem_u32(p)) : "memory");
-  return v;
-}
-
 // Warp arrival on barrier `bar` of the CTA that issues the MMAs: this CTA's
 // own, or for a CTA pair the leader's barrier at the same offset.
 template <bool PAIR>
@@ -808,16 +800,16 @@ __device__ __forceinline__ void tc_softmax(const TcParams& p, const TcBars<D, NQ
       const float alpha = (m_new == -INFINITY) ? 1.f : ex2(m - m_new);
       float nb = (m_new == -INFINITY) ? 0.f : -m_new;
       if (j > 0) {
-        float* slot = alpha_s + (a_pub & 1) * 128 + r;
-        *slot = alpha;
-        warp_arrive(bar.a_full(ot, a_pub & 1));
+        alpha_s[(a_pub & 1) * 128 + r] = alpha;
+        // The exponentials below are made to depend on the arrival's state
+        // word (masked to zero), so the arrival is issued before them and the
+        // correction warpgroup rescales O while they run; otherwise the
+        // compiler may schedule the arrival after the exponentials, since
+        // nothing in this warp depends on it.  (A read-back of alpha from
+        // shared memory would order them too, but waits behind the tensor
+        // core's operand reads.)
+        nb = fmaf(0.f, __uint_as_float(warp_arrive_token(bar.a_full(ot, a_pub & 1))), nb);
         ++a_pub;
-        // The exponentials below are made to depend on a load that follows the
-        // arrival (alpha read back, times zero: alpha is finite), so the
-        // arrival is issued before them and the correction warpgroup rescales
-        // O while they run; otherwise the compiler may schedule the arrival
-        // after the exponentials, since nothing in this warp depends on it.
-        nb = fmaf(0.f, ld_shared_volatile(slot), nb);
       }
       const uint64_t nb2 = f2_pack(nb, nb);
       uint64_t acc[4];

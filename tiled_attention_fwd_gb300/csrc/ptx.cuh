@@ -194,6 +194,24 @@ __device__ __forceinline__ void warp_arrive_elect(uint32_t bar) {
       : "memory");
 }
 
+// warp_arrive_elect that also returns a word which is zero but which the
+// compiler sees computed from the arrival (its state operand): code that uses
+// it is scheduled after the arrival.
+__device__ __forceinline__ uint32_t warp_arrive_token(uint32_t bar) {
+  __syncwarp();
+  uint64_t state = 0;
+  asm volatile(
+      "{\n\t.reg .pred PE;\n\t"
+      "elect.sync _|PE, 0xffffffff;\n\t"
+      "@PE mbarrier.arrive.shared::cta.b64 %0, [%1];\n\t}"
+      : "+l"(state)
+      : "r"(bar)
+      : "memory");
+  uint32_t z;
+  asm("and.b32 %0, %1, 0;" : "=r"(z) : "r"(static_cast<uint32_t>(state)));
+  return z;
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
