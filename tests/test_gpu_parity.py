@@ -67,6 +67,23 @@ def test_bf16_large_logits_several_units(d):
         _assert(check_full(w), f"qk3 d={d} causal={causal}")
 
 
+@pytest.mark.parametrize("d", [32, 64, 128, 256])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_row_max_is_per_row(d, causal):
+    """Every 32nd query row (so one row in each warp of 32 TMEM lanes) scaled
+    by 60: its row max reaches 120 to 450 in log2 units while its neighbours'
+    stay below 8, a gap above 150 in at least 62 of the 66 warps of each case.
+    Softmax does not depend on which shift is subtracted, so only the size of
+    the shift can show: a row max taken over more than the row's own columns
+    (over the warp's lanes, say) would put every P of the other rows of such a
+    warp below 2^-150, which flushes to 0, and leave their O and L not finite."""
+    w = Workload("bf16_rowmax", 1, 3, 700, d, "bf16", causal, seed=21 + d)
+    q, k, v = make_qkv(w)
+    q = q.clone()
+    q[:, :, ::32, :] = (q[:, :, ::32, :].float() * 60.0).to(q.dtype)
+    _assert(check_full(w, q, k, v), f"row max d={d} causal={causal}")
+
+
 def test_bf16_many_units_per_cta():
     """More work units than SMs, so every persistent CTA runs several units."""
     w = Workload("bf16_units", 3, 64, 700, 64, "bf16", True, seed=5)

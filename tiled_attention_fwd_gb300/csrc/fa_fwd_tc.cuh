@@ -755,13 +755,16 @@ __device__ __forceinline__ void tc_softmax(const TcParams& p, const TcBars<D, NQ
       tc_fence_after();
       const uint32_t ts = tmem + lane_off + C::TM_S + buf * C::TM_SB;
 
+      // S is loaded with the maximum of each 32-column chunk (the TMEM load's
+      // own reduction), which is the row max wherever no column is masked.
       float s[C::BK];
+      float cmax[C::BK / 32];
       {
         uint32_t raw_s[C::BK / 32][32];
 #pragma unroll
-        for (int c = 0; c < C::BK / 32; ++c) tmem_ld32(ts + c * 32, raw_s[c]);
+        for (int c = 0; c < C::BK / 32; ++c) tmem_ld32_max(ts + c * 32, raw_s[c], cmax[c]);
 #pragma unroll
-        for (int c = 0; c < C::BK / 32; ++c) tmem_wait_ld(raw_s[c]);
+        for (int c = 0; c < C::BK / 32; ++c) tmem_wait_ld(raw_s[c], cmax[c]);
 #pragma unroll
         for (int c = 0; c < C::BK / 32; ++c)
 #pragma unroll
@@ -769,6 +772,7 @@ __device__ __forceinline__ void tc_softmax(const TcParams& p, const TcBars<D, NQ
       }
       const int key0 = j * C::BK;
       const bool need_mask = (CAUSAL && key0 + C::BK - 1 > row0) || (key0 + C::BK > p.Nk);
+      float rmax;
       if (need_mask) {
         // Column c of this row is visible iff c <= lim; 32-column blocks that
         // every lane of the warp sees whole are skipped (warp-uniform test).
@@ -782,19 +786,23 @@ __device__ __forceinline__ void tc_softmax(const TcParams& p, const TcBars<D, NQ
               if (32 * cb + i > lim) s[32 * cb + i] = -INFINITY;
           }
         }
-      }
-      // Row max: 8 chains of three-input maxima over interleaved columns.
-      constexpr int KC = C::BK / 8;
-      float mx[8];
+        // Row max of the masked row: 8 chains of three-input maxima over interleaved columns.
+        constexpr int KC = C::BK / 8;
+        float mx[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        float v = fmax3(s[i], s[i + 8], s[i + 16]);
+        for (int i = 0; i < 8; ++i) {
+          float v = fmax3(s[i], s[i + 8], s[i + 16]);
 #pragma unroll
-        for (int k = 3; k + 1 < KC; k += 2) v = fmax3(v, s[i + 8 * k], s[i + 8 * (k + 1)]);
-        if ((KC - 3) % 2 == 1) v = fmaxf(v, s[i + 8 * (KC - 1)]);
-        mx[i] = v;
+          for (int k = 3; k + 1 < KC; k += 2) v = fmax3(v, s[i + 8 * k], s[i + 8 * (k + 1)]);
+          if ((KC - 3) % 2 == 1) v = fmaxf(v, s[i + 8 * (KC - 1)]);
+          mx[i] = v;
+        }
+        rmax = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7]));
+      } else {
+        rmax = cmax[0];
+#pragma unroll
+        for (int c = 1; c < C::BK / 32; ++c) rmax = fmaxf(rmax, cmax[c]);
       }
-      const float rmax = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7]));
       const float m_new = fmaxf(m, rmax * sl2);
       // alpha = exp2(m_old - m_new): 0 on the first tile, exactly 1 when the max did not grow.
       const float alpha = (m_new == -INFINITY) ? 1.f : ex2(m - m_new);
