@@ -110,6 +110,15 @@ struct TcCfg {
   // keys are half as many MMAs as in bf16, and the split measured 1.1-1.3 %
   // slower on all three d = 128 e4m3 workloads.
   static constexpr bool PV_SPLIT = (NQT == 2 && D == 128 && !FP8);
+  // Lazy row max (bf16 two-tile kernels): the reference max m moves only when
+  // a key tile's row max exceeds it by more than MAX_SLACK (log2 units), so
+  // P <= 2^MAX_SLACK and most steps need no rescale of O.  The largest P of a
+  // step is then not exactly 1 and its bf16 rounding would no longer be
+  // matched by l (the fp32 sum), so O's normaliser adds, per step, that P's
+  // rounding residual (bf16(p) - p, computed from the row max exactly as the
+  // exponential loop computes it); L keeps the fp32 sum.
+  static constexpr bool LAZY_MAX = (NQT == 2 && !FP8);
+  static constexpr float MAX_SLACK = 8.f;
   // Shared memory: [Q tiles][K/V stages][misc]; misc = barriers, alpha, m/l, TMEM address, abort flag.
   static constexpr int MISC = 7168;
   static constexpr int SMEM_LIMIT = 227 * 1024;
@@ -746,6 +755,7 @@ __device__ __forceinline__ void tc_softmax(const TcParams& p, const TcBars<D, NQ
     const int row = row0 + r;
     float m = -INFINITY;  // running max of scaled logits, log2 units
     float l = 0.f;        // running sum of exp2(x - m)
+    float lres = 0.f;     // lazy max: running sum of the steps' largest-P rounding residuals
     for (int j = 0; j < n; ++j) {
       const int buf = (C::NQT == 2) ? wg : static_cast<int>(s_waits & 1);
       const uint32_t par = (C::NQT == 2) ? (s_waits & 1) : ((s_waits >> 1) & 1);
@@ -803,9 +813,17 @@ __device__ __forceinline__ void tc_softmax(const TcParams& p, const TcBars<D, NQ
 #pragma unroll
         for (int c = 1; c < C::BK / 32; ++c) rmax = fmaxf(rmax, cmax[c]);
       }
-      const float m_new = fmaxf(m, rmax * sl2);
-      // alpha = exp2(m_old - m_new): 0 on the first tile, exactly 1 when the max did not grow.
-      const float alpha = (m_new == -INFINITY) ? 1.f : ex2(m - m_new);
+      float m_new, alpha;
+      if constexpr (C::LAZY_MAX) {
+        const float rm = rmax * sl2;
+        m_new = (rm > m + C::MAX_SLACK) ? rm : m;
+        // alpha = exp2(m_old - m_new): 0 on the first tile, exactly 1 while m stays.
+        alpha = (m_new == m) ? 1.f : ex2(m - m_new);
+      } else {
+        m_new = fmaxf(m, rmax * sl2);
+        // alpha = exp2(m_old - m_new): 0 on the first tile, exactly 1 when the max did not grow.
+        alpha = (m_new == -INFINITY) ? 1.f : ex2(m - m_new);
+      }
       float nb = (m_new == -INFINITY) ? 0.f : -m_new;
       if (j > 0) {
         alpha_s[(a_pub & 1) * 128 + r] = alpha;
@@ -820,6 +838,11 @@ __device__ __forceinline__ void tc_softmax(const TcParams& p, const TcBars<D, NQ
         ++a_pub;
       }
       const uint64_t nb2 = f2_pack(nb, nb);
+      if constexpr (C::LAZY_MAX) {
+        const float pmax = ex2(fmaf(rmax, sl2, nb));  // the step's largest P, as the loop below computes it
+        const float pr = __uint_as_float(pack_bf16x2(pmax, 0.f) << 16);
+        lres = lres * alpha + (pr - pmax);
+      }
       uint64_t acc[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[i] = 0ull;  // (0.f, 0.f)
@@ -869,8 +892,10 @@ __device__ __forceinline__ void tc_softmax(const TcParams& p, const TcBars<D, NQ
       arrive_issuer<C::PAIR>(C::NQT == 2 ? bar.pv_go(ot, C::PV_SPLIT ? 1 : 0) : bar.pv_go(0, (s_waits - 1) & 1));
     }
     if (!ok) break;
-    stat_m[(uk & 1) * 256 + r] = m;
-    stat_l[(uk & 1) * 256 + r] = l;
+    // Lazy max: the row's log2-sum-exp2 (from the fp32 sum) and O's
+    // normaliser; otherwise m and l.
+    stat_m[(uk & 1) * 256 + r] = C::LAZY_MAX ? m + log2f(l) : m;
+    stat_l[(uk & 1) * 256 + r] = C::LAZY_MAX ? l + lres : l;
     warp_arrive(bar.l_full(ot));
   }
 }
@@ -1008,7 +1033,8 @@ __device__ __forceinline__ void tc_correction(const TcParams& p, const CUtensorM
         }
       }
     }
-    if (row < p.Nq) p.lse[static_cast<size_t>(w.bh) * p.Nq + row] = (mrow + log2f(lrow)) * 0.69314718055994531f;
+    if (row < p.Nq)
+      p.lse[static_cast<size_t>(w.bh) * p.Nq + row] = (C::LAZY_MAX ? mrow : mrow + log2f(lrow)) * 0.69314718055994531f;
     return true;
   };
 
