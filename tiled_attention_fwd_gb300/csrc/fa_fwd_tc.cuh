@@ -161,18 +161,19 @@ struct TcCfg {
   static constexpr int LOAD_WARP = MMA_WARP + 1;
   static constexpr int THREADS = 32 * (SOFTMAX_WARPS + 8);  // + correction WG + MMA/TMA WG
   // Register split (d <= 128 and CTA pairs).  Two tiles, 512 threads launched at 128
-  // registers each: softmax 176 and 160 between the correction and the
-  // MMA/TMA warpgroups: 80 / 80, or 72 / 88 where that measured faster
-  // (contiguous bf16 d = 64; the strided and e4m3 epilogues need the correction's 80);
-  // 2*128*176 + 128*160 = 65536.  One tile, 384 threads launched at 168:
+  // registers each: bf16 softmax 184 (its lazy row max keeps one more value
+  // across the exponential loop; at 176 it spilled 8 bytes), correction 80,
+  // MMA/TMA 64 (2*128*184 + 128*144 = 65536; 72 / 72 measured slower);
+  // e4m3 softmax 176, correction 80, MMA/TMA 80 (2*128*176 + 128*160 = 65536).
+  // One tile, 384 threads launched at 168:
   // softmax 208, correction 152, MMA/TMA 144; 128*(208 + 296) = 64512
   // (CTA pairs at d = 256: correction 160 for its 256-column rescale, 136).
   // d = 256 on one CTA (64-column S) fits 168 everywhere and is not split.
   static constexpr bool SPLIT_REGS = (D <= 128 || PAIR);
-  static constexpr uint32_t REG_SOFTMAX = (NQT == 2) ? 176 : 208;
-  static constexpr uint32_t REG_CORR_OTHER = (NQT == 2) ? 160 : 296;
+  static constexpr uint32_t REG_SOFTMAX = (NQT == 2) ? (FP8 ? 176 : 184) : 208;
+  static constexpr uint32_t REG_CORR_OTHER = (NQT == 2) ? (FP8 ? 160 : 144) : 296;
   static constexpr __host__ __device__ uint32_t reg_corr(bool strided) {
-    return NQT == 1 ? (PAIR ? 160 : 152) : ((!strided && D == 64 && !FP8) ? 72 : 80);
+    return NQT == 1 ? (PAIR ? 160 : 152) : 80;
   }
   static constexpr int LAUNCH_REGS = 65536 / THREADS > 255 ? 255 : (65536 / THREADS) & ~7;
   static_assert(!SPLIT_REGS || NQT * 128 * REG_SOFTMAX + 128 * REG_CORR_OTHER <= THREADS * LAUNCH_REGS,
