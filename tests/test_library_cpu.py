@@ -103,8 +103,7 @@ def test_missing_library_fails_loudly(tmp_path):
 
 def test_tensor_core_kernels_fit_their_register_split():
     """The two-tile d <= 128 kernels (bf16 and e4m3) launch 512 threads at 128 registers and re-split them
-    (bf16: 184 x 256 softmax + 144 x 128 correction and MMA/TMA, 80/64; e4m3: 176 x 256 + 160 x 128,
-    80/80; 65536 either way); the
+    (184 x 256 softmax + 144 x 128 correction and MMA/TMA, 80/64 = 65536); the
     single-tile d <= 128 kernels launch 384 threads at 168 (208 softmax, 152 correction,
     144 MMA/TMA); any other launch count would stall setmaxnreg, and none of them may spill."""
     if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):

@@ -110,14 +110,15 @@ struct TcCfg {
   // keys are half as many MMAs as in bf16, and the split measured 1.1-1.3 %
   // slower on all three d = 128 e4m3 workloads.
   static constexpr bool PV_SPLIT = (NQT == 2 && D == 128 && !FP8);
-  // Lazy row max (bf16 two-tile kernels): the reference max m moves only when
-  // a key tile's row max exceeds it by more than MAX_SLACK (log2 units), so
-  // P <= 2^MAX_SLACK and most steps need no rescale of O.  The largest P of a
-  // step is then not exactly 1 and its bf16 rounding would no longer be
-  // matched by l (the fp32 sum), so O's normaliser adds, per step, that P's
-  // rounding residual (bf16(p) - p, computed from the row max exactly as the
-  // exponential loop computes it); L keeps the fp32 sum.
-  static constexpr bool LAZY_MAX = (NQT == 2 && !FP8);
+  // Lazy row max (two-tile kernels): the reference max m moves only when a
+  // key tile's row max exceeds it by more than MAX_SLACK (log2 units), so
+  // P <= 2^MAX_SLACK (below e4m3's 448) and most steps need no rescale of O.
+  // The largest P of a step is then not exactly 1 and its rounding to P's
+  // type would no longer be matched by l (the fp32 sum), so O's normaliser
+  // adds, per step, that P's rounding residual (round(p) - p, p computed from
+  // the row max exactly as the exponential loop computes it); L keeps the
+  // fp32 sum.
+  static constexpr bool LAZY_MAX = (NQT == 2);
   static constexpr float MAX_SLACK = 8.f;
   // Shared memory: [Q tiles][K/V stages][misc]; misc = barriers, alpha, m/l, TMEM address, abort flag.
   static constexpr int MISC = 7168;
@@ -161,17 +162,16 @@ struct TcCfg {
   static constexpr int LOAD_WARP = MMA_WARP + 1;
   static constexpr int THREADS = 32 * (SOFTMAX_WARPS + 8);  // + correction WG + MMA/TMA WG
   // Register split (d <= 128 and CTA pairs).  Two tiles, 512 threads launched at 128
-  // registers each: bf16 softmax 184 (its lazy row max keeps one more value
+  // registers each: softmax 184 (its lazy row max keeps one more value
   // across the exponential loop; at 176 it spilled 8 bytes), correction 80,
-  // MMA/TMA 64 (2*128*184 + 128*144 = 65536; 72 / 72 measured slower);
-  // e4m3 softmax 176, correction 80, MMA/TMA 80 (2*128*176 + 128*160 = 65536).
+  // MMA/TMA 64 (2*128*184 + 128*144 = 65536; 72 / 72 measured slower).
   // One tile, 384 threads launched at 168:
   // softmax 208, correction 152, MMA/TMA 144; 128*(208 + 296) = 64512
   // (CTA pairs at d = 256: correction 160 for its 256-column rescale, 136).
   // d = 256 on one CTA (64-column S) fits 168 everywhere and is not split.
   static constexpr bool SPLIT_REGS = (D <= 128 || PAIR);
-  static constexpr uint32_t REG_SOFTMAX = (NQT == 2) ? (FP8 ? 176 : 184) : 208;
-  static constexpr uint32_t REG_CORR_OTHER = (NQT == 2) ? (FP8 ? 160 : 144) : 296;
+  static constexpr uint32_t REG_SOFTMAX = (NQT == 2) ? 184 : 208;
+  static constexpr uint32_t REG_CORR_OTHER = (NQT == 2) ? 144 : 296;
   static constexpr __host__ __device__ uint32_t reg_corr(bool strided) {
     return NQT == 1 ? (PAIR ? 160 : 152) : 80;
   }
@@ -841,7 +841,7 @@ __device__ __forceinline__ void tc_softmax(const TcParams& p, const TcBars<D, NQ
       const uint64_t nb2 = f2_pack(nb, nb);
       if constexpr (C::LAZY_MAX) {
         const float pmax = ex2(fmaf(rmax, sl2, nb));  // the step's largest P, as the loop below computes it
-        const float pr = __uint_as_float(pack_bf16x2(pmax, 0.f) << 16);
+        const float pr = C::FP8 ? round_e4m3(pmax) : __uint_as_float(pack_bf16x2(pmax, 0.f) << 16);
         lres = lres * alpha + (pr - pmax);
       }
       uint64_t acc[4];

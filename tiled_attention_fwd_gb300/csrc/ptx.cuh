@@ -883,6 +883,20 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // Four fp32 values to four e4m3 bytes (round to nearest even, saturating to
 // +-448); `p0` in bits 0..7 (the lowest K index first, as a TMEM A operand of
 // kind::f8f6f4 holds four consecutive K elements per 32-bit column).
+// x rounded to e4m3 as pack_e4m3x4 rounds it (nearest even, saturating),
+// back in fp32 (e4m3 -> f16 -> f32 are exact).
+__device__ __forceinline__ float round_e4m3(float x) {
+  float r;
+  asm("{\n\t.reg .b16 b, lo, hi;\n\t.reg .b32 h2;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 b, %1, %1;\n\t"
+      "cvt.rn.f16x2.e4m3x2 h2, b;\n\t"
+      "mov.b32 {lo, hi}, h2;\n\t"
+      "cvt.f32.f16 %0, lo;\n\t}"
+      : "=f"(r)
+      : "f"(x));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t pack_e4m3x4(float p0, float p1, float p2, float p3) {
   uint32_t r;
   asm("{\n\t.reg .b16 lo, hi;\n\t"
