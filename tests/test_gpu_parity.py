@@ -5,6 +5,8 @@ configuration of the benchmark and compare sampled rows that the oracle
 computes one by one, plus properties of every output.  Outputs are poisoned
 with NaN before each launch so an unwritten row fails.
 """
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -82,6 +84,32 @@ def test_bf16_row_max_is_per_row(d, causal):
     q = q.clone()
     q[:, :, ::32, :] = (q[:, :, ::32, :].float() * 60.0).to(q.dtype)
     _assert(check_full(w, q, k, v), f"row max d={d} causal={causal}")
+
+
+@pytest.mark.parametrize("d", [32, 64, 128])
+def test_bf16_dominant_key_after_the_reference_max(d):
+    """Every row's logits (log2 units): 20 at key 5, about 25.4 at key 300
+    (after K's bf16 rounding), about -10 elsewhere, so the two-tile kernels'
+    lazy reference max is set by key 5 and stays there (300 is within its
+    slack of 8): key 300 dominates with a weight near 2^5.4 that bf16 does not
+    hold exactly, and its value row has entries near +-6.  This runs the
+    largest-P rounding residual on a row it matters for and requires parity;
+    tests/test_lazy_max_rounding.py shows on the CPU that the lazy max breaks
+    the bound without that residual.  40 heads of 512 rows are 80 units of
+    256 rows, so the two-tile kernel runs, not the small-problem one."""
+    w = Workload("bf16_lazy", 1, 40, 512, d, "bf16", False, seed=31 + d)
+    g = torch.Generator().manual_seed(31 + d)
+    logit2 = torch.randn(w.B, w.H, w.N, generator=g) - 10.0
+    logit2[:, :, 5] = 20.0
+    logit2[:, :, 300] = 25.37
+    q = torch.zeros(w.B, w.H, w.N, d)
+    q[..., 0] = 1.0
+    k = torch.zeros(w.B, w.H, w.N, d)
+    k[..., 0] = logit2 * math.log(2.0) / w.scale  # S * scale = the natural-log logit
+    v = torch.randn(w.B, w.H, w.N, d, generator=g)
+    v[:, :, 300, :] = torch.sign(torch.randn(w.B, w.H, d, generator=g)) * (5.5 + 0.5 * torch.rand(w.B, w.H, d, generator=g))
+    q, k, v = (t.to(torch.bfloat16) for t in (q, k, v))
+    _assert(check_full(w, q, k, v), f"dominant key d={d}")
 
 
 def test_bf16_many_units_per_cta():
